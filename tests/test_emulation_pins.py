@@ -1,0 +1,92 @@
+"""Pins of the blocked BF16 emulation (the oracle's second program)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from oracle import emulation as E
+from numerics_tcgen05_tmem_gb300 import inputs
+
+
+def test_round_bf16_ties_to_even_and_matches_torch():
+    one = np.float32(1.0)
+    halfway = np.float32(1.0 + 2.0 ** -8)          # midway between 1 and 1 + 2^-7
+    assert E.round_bf16(np.array([halfway]))[0] == one
+    upper = np.float32(1.0 + 3 * 2.0 ** -8)         # midway between 1+2^-7 and 1+2^-6 -> even
+    assert E.round_bf16(np.array([upper]))[0] == np.float32(1.0 + 2.0 ** -6)
+    x = np.random.default_rng(1).standard_normal(100000).astype(np.float32) * 10
+    ref = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(E.round_bf16(x), ref)
+
+
+def test_exp_margin_near_one_clears_bf16_rounding():
+    # On the dyadic grid the nearest non-tie score sits 2^-9 (scaled) below the
+    # maximum.  exp(-2^-9) lies ~1.9e-6 above the BF16 midpoint 1 - 2^-9, so it
+    # rounds to 1.0; two grid steps below (exp(-2^-8)) it does not.  Both sit
+    # far from the midpoint compared with any FP32 exp error, so exact-1.0
+    # counts are the same whichever correctly rounded exp is used.
+    mid = 1.0 - 2.0 ** -9
+    p1 = np.float32(np.exp(-2.0 ** -9))
+    p2 = np.float32(np.exp(-2.0 ** -8))
+    assert E.round_bf16(np.array([p1]))[0] == np.float32(1.0)
+    assert E.round_bf16(np.array([p2]))[0] == np.float32(1.0 - 2.0 ** -8)
+    assert float(p1) - mid > 1.5e-6 and mid - float(p2) > 1e-3
+
+
+@pytest.mark.parametrize("block_n", [1, 3, 16, 128])
+@pytest.mark.parametrize("stable", [0, 1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp64_recurrence_equals_one_shot(block_n, stable, causal):
+    # ijyty.com §2.1: the online softmax over key blocks reaches the one-shot result
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((1, 2, 45, 8)) * 2
+    k = rng.standard_normal((1, 2, 45, 8)) * 2
+    k[0, :, 10] = k[0, :, 3]
+    v = rng.standard_normal((1, 2, 45, 8))
+    ref = A.forward(q, k, v, 0.5, causal)
+    em = E.blocked_forward(q, k, v, 0.5, causal, stable=stable, block_n=block_n, precision="fp64")
+    np.testing.assert_allclose(em["o"], ref["o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(em["lse"], ref["lse"], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("block_n", [1, 7, 32, 128])
+def test_running_tie_state_equals_whole_row(block_n):
+    w = inputs.tiny_ties()
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=1)
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, block_n=block_n)
+    np.testing.assert_array_equal(em["rm"].astype(np.float64), ref["rm"])
+    np.testing.assert_array_equal(em["rs"], ref["rs"])
+    np.testing.assert_array_equal(em["branch"], ref["branch"])
+
+
+def test_plain_mode_produces_exact_ones_at_repeated_maxima():
+    # ijyty.com §2.2/§3.1: a repeated row maximum gives P~ entries of exactly 1.0
+    w = inputs.tiny_ties()
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=0)
+    rs, ones = em["rs"], em["ones"]
+    assert np.all(ones[rs > 1] >= rs[rs > 1])
+    assert np.all(ones >= 1)           # the maximum itself always gives exp(0) = 1
+    assert np.sum(rs > 1) >= 5
+
+
+def test_stable_mode_removes_exact_ones():
+    # web578.cn "mechanism 2": with a repeated maximum the shift moves so the
+    # exponent at the maximum is strictly below 1 -> no exact 1.0 after BF16 rounding
+    w = inputs.tiny_ties()
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, beta=1.25)
+    rm, rs, m = em["rm"].astype(np.float64), em["rs"], em["m"].astype(np.float64)
+    margin = w.scale * np.abs(m - rm)
+    sel = (rs > 1) & (rm != 0) & (margin >= 2.0 ** -7)
+    assert sel.sum() >= 4
+    assert np.all(em["ones"][sel] == 0)
+    # rows with a unique maximum keep their single exact 1.0
+    assert np.all(em["ones"][rs == 1] >= 1)
+
+
+def test_bf16_emulation_within_contract_tolerance():
+    w = inputs.gpt2_small(B=1, H=2, N=300)
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=1)
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=1)
+    rel = np.linalg.norm(em["o"] - ref["o"]) / np.linalg.norm(ref["o"])
+    assert rel <= 1e-2
+    assert np.max(np.abs(em["lse"] - ref["lse"])) <= 1e-3
