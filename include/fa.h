@@ -1,0 +1,135 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) stabilised BF16 FlashAttention library.
+ *
+ * The library computes softmax attention O = softmax(scale * Q K^T) V and its
+ * gradients with hand-written tcgen05/TMA kernels.  It follows these pages:
+ *
+ *   [ijyty]  ijyty.com/news/896914 (BF16 FlashAttention numerical stability):
+ *            §2.1 tiled online softmax -- running row max m, running sum l,
+ *            O rescaled by exp(m_prev - m), P~ = exp(S - m), O += P~ V,
+ *            final O = diag(l)^-1 O; §3.1 delta = rowsum(dO o O) in the
+ *            backward; §4.1/§4.2 the stabilised safe softmax (a repeated row
+ *            maximum moves the shift to beta*rm for rm > 0 or to 0 for rm < 0;
+ *            beta in [1.1, 1.5], 1.25 recommended); §7.1 the monitor
+ *            (S == rowmax(S)).sum().
+ *   [jsqmd]  "Flash Attention低精度训练稳定性优化实践" §3.2: QK^T accumulated in
+ *            FP32, softmax in FP32, the product with V in BF16; §3.3 the
+ *            running max / log-sum-exp bookkeeping.
+ *   [cnnet]  "FlashAttention 训练时为什么会梯度爆炸？" §2: the backward recomputes
+ *            the forward's probabilities from Q, K, V instead of storing them;
+ *            §3.1 Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V.
+ *   [web578] "為什么BF16的FlashAttention會把訓練「炸掉」？" mechanism 2: detect a
+ *            repeated row maximum and shift so the exponent at the maximum is
+ *            strictly below 1.
+ *
+ * Conventions shared by every entry point
+ *   - Tensors q, k, v, o, dO, dq, dk, dv are BF16, contiguous [B, H, N, d]
+ *     row-major (d fastest).  lse and delta are FP32 [B, H, N].  All are
+ *     DEVICE pointers, 16-byte aligned, owned by the caller.
+ *   - d must be 64 or 128; N >= 1; B, H >= 1; B*H*N < 2^31.
+ *   - scale must be finite and > 0 (the pages advise choosing it by
+ *     experiment rather than fixing 1/sqrt(d) [jsqmd §5], so it is explicit).
+ *   - causal != 0 means query i sees keys j <= i (top-left aligned).
+ *   - lse is the natural-log logsumexp of the scaled logits scale*q.k.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The return value reports argument and launch errors
+ *     only; errors raised on the device (a bounded wait that timed out) are
+ *     read with fa_device_status().
+ *   - The library allocates nothing per call.  It keeps one 4-byte status
+ *     word per device, allocated on first use.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer, bad scale/beta */
+  FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d not in {64, 128}) */
+  FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see fa_last_error() */
+  FA_ERR_TIMEOUT = 4,       /* (fa_device_status) a kernel's bounded wait ran out */
+  FA_ERR_DEVICE_BOUNDS = 5  /* (fa_device_status) a debug bounds check fired */
+} fa_status;
+
+/* Shift branch codes written to fa_row_stats.row_branch. */
+enum { FA_BRANCH_RM = 0, FA_BRANCH_BETA = 1, FA_BRANCH_ZERO = 2 };
+
+/*
+ * Optional per-row statistics of the forward ([ijyty §7.1] monitor; [jsqmd §5]
+ * "watch the max/min of the softmax input").  Each pointer is a device array
+ * of B*H*N entries or NULL (not written).
+ *   row_max_raw : rm, the largest visible raw score q.k (before scale)
+ *   row_ties    : rs, how many visible keys reach rm exactly (FP32 equality)
+ *   row_branch  : which shift the stabilised rule chose (FA_BRANCH_*); 0 in plain mode
+ *   row_ones    : how many visible BF16 P~ entries of the row were exactly 1.0
+ */
+typedef struct {
+  float* row_max_raw;
+  int32_t* row_ties;
+  int8_t* row_branch;
+  int32_t* row_ones;
+} fa_row_stats;
+
+/*
+ * fa_fwd -- attention forward ([ijyty §2.1], [cnnet §3.1]).
+ *   q, k, v : inputs, BF16 [B,H,N,d]
+ *   o       : output, BF16 [B,H,N,d]
+ *   lse     : output, FP32 [B,H,N]
+ *   stable  : 0 = plain safe softmax (m = running row max);
+ *             1 = stabilised shift [ijyty §4.1] with a running tie count over
+ *                 all visible keys seen so far (m = beta*rm if rm > 0 and the
+ *                 maximum repeats, 0 if rm < 0 and it repeats, else rm);
+ *   beta    : shift factor for stable = 1; finite and >= 1 (ignored when stable = 0)
+ *   stats   : optional per-row statistics (NULL = none)
+ * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           int causal, float scale, int stable, float beta, const fa_row_stats* stats, void* stream);
+
+/*
+ * fa_bwd_workspace_size -- bytes of device scratch fa_bwd needs: an FP32
+ * [B,H,N,d] dQ accumulator plus an FP32 [B,H,N] delta, each rounded up to
+ * 256 bytes.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_bwd -- attention backward by recomputation ([cnnet §2], [ijyty §3.1]).
+ *   q, k, v, o, lse, dO : forward inputs/outputs and the output gradient
+ *   dq, dk, dv          : outputs, BF16 [B,H,N,d]
+ *   delta_out           : optional FP32 [B,H,N] copy of delta = rowsum(dO o O) (NULL = none)
+ *   workspace           : caller-owned device scratch of at least
+ *                         fa_bwd_workspace_size(B,H,N,d) bytes, 256-byte aligned;
+ *                         its contents on entry do not matter
+ * The backward uses only o and lse from the forward, so it is the same for
+ * plain and stabilised forwards.
+ * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+           void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N, int d, int causal,
+           float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_device_status -- synchronise `stream`, then return and clear the current
+ * device's status word: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_BOUNDS
+ * (FA_ERR_CUDA if the synchronisation itself fails).
+ */
+int fa_device_status(void* stream);
+
+/* Message for the last non-OK return on the calling thread ("" if none). */
+const char* fa_last_error(void);
+
+/* Library version string. */
+const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

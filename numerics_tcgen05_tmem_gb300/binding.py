@@ -1,0 +1,160 @@
+"""Thin ctypes binding of ``libfa.so`` (see ``include/fa.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the stream.
+There is no fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_DEVICE_BOUNDS = 5
+
+# every symbol include/fa.h declares
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_device_status", "fa_last_error", "fa_version")
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"fa error {code}: {msg}")
+        self.code = code
+
+
+class RowStats(ctypes.Structure):
+    _fields_ = [("row_max_raw", ctypes.c_void_p), ("row_ties", ctypes.c_void_p),
+                ("row_branch", ctypes.c_void_p), ("row_ones", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the library (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m numerics_tcgen05_tmem_gb300.build`")
+    L = ctypes.CDLL(path)
+    vp, ci, cf, cs = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, ctypes.POINTER(RowStats), vp]
+    L.fa_fwd.restype = ci
+    L.fa_bwd_workspace_size.argtypes = [ci, ci, ci, ci]
+    L.fa_bwd_workspace_size.restype = cs
+    L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, cs, vp]
+    L.fa_bwd.restype = ci
+    L.fa_device_status.argtypes = [vp]
+    L.fa_device_status.restype = ci
+    L.fa_last_error.argtypes = []
+    L.fa_last_error.restype = ctypes.c_char_p
+    L.fa_version.argtypes = []
+    L.fa_version.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return load().fa_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != FA_OK:
+        raise FAError(rc, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_qkv(*ts):
+    for t in ts:
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and t.dim() == 4):
+            raise ValueError("expected contiguous CUDA bfloat16 tensors of shape [B, H, N, d]")
+    if any(t.shape != ts[0].shape for t in ts):
+        raise ValueError("q, k, v (and o, dO) must have the same shape")
+
+
+# ----------------------------------------------------------------- raw C calls
+
+def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stable: int, beta: float, stats=None, stream=None) -> int:
+    B, H, N, d = q.shape
+    st = None
+    if stats is not None:
+        st = RowStats(*(None if stats.get(n) is None else stats[n].data_ptr()
+                        for n in ("row_max_raw", "row_ties", "row_branch", "row_ones")))
+    return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
+                         float(scale), int(stable), float(beta), ctypes.byref(st) if st is not None else None,
+                         _stream(stream))
+
+
+def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, delta, causal: bool, scale: float, workspace, stream=None) -> int:
+    B, H, N, d = q.shape
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                         _ptr(delta), B, H, N, d, int(bool(causal)), float(scale), _ptr(workspace), nbytes,
+                         _stream(stream))
+
+
+def fa_device_status(stream=None) -> int:
+    return load().fa_device_status(_stream(stream))
+
+
+# ----------------------------------------------------------------- tensor-level helpers
+
+def forward(q, k, v, causal: bool = True, scale=None, stable: int = 1, beta: float = 1.25, stats: bool = False,
+            stream=None):
+    """Returns (o, lse) or (o, lse, stats_dict); outputs are freshly allocated."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    sd = None
+    if stats:
+        sd = {"row_max_raw": torch.empty((B, H, N), device=q.device, dtype=torch.float32),
+              "row_ties": torch.empty((B, H, N), device=q.device, dtype=torch.int32),
+              "row_branch": torch.empty((B, H, N), device=q.device, dtype=torch.int8),
+              "row_ones": torch.empty((B, H, N), device=q.device, dtype=torch.int32)}
+    _check(fa_fwd(q, k, v, o, lse, causal, scale, stable, beta, sd, stream))
+    return (o, lse, sd) if stats else (o, lse)
+
+
+def backward(q, k, v, o, lse, do, causal: bool = True, scale=None, workspace=None, want_delta: bool = False,
+             stream=None):
+    """Returns (dq, dk, dv) or (dq, dk, dv, delta)."""
+    _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(B, H, N, d), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if want_delta else None
+    _check(fa_bwd(q, k, v, o, lse, do, dq, dk, dv, delta, causal, scale, workspace, stream))
+    return (dq, dk, dv, delta) if want_delta else (dq, dk, dv)
+
+
+def device_status(stream=None):
+    """Synchronise and raise if a kernel reported a device-side error."""
+    _check(fa_device_status(stream))

@@ -1,0 +1,522 @@
+// Attention backward for sm_103a by recomputation.
+//
+// The backward re-derives the attention probabilities from Q, K and the saved
+// log-sum-exp instead of storing them ("FlashAttention 训练时为什么会梯度爆炸？",
+// §2), and uses delta = rowsum(dO o O) (ijyty.com/news/896914, §3.1).  The
+// gradient formulas, which the pages do not print, are the calculus of
+// O = softmax(scale Q K^T) V:
+//   P = exp(scale S - lse),  dV = P^T dO,  dP = dO V^T,
+//   dS = P o (dP - delta),   dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Three kernels on the caller's stream:
+//   fa_bwd_preprocess: delta_i = sum_c dO_ic O_ic (FP32) and dQ_acc = 0
+//   fa_bwd_main:       one CTA per (b, h, 128-key tile); loops over query tiles
+//   fa_bwd_dq_convert: dq = bf16(scale * dQ_acc)
+//
+// fa_bwd_main CTA organisation:
+//   warps 0-3  "softmax" warpgroup: thread = key row (TMEM lane) of the tile;
+//              P^T = exp2(S^T c - lse_q log2 e) into TMEM (BF16) for the dV MMA,
+//              dS^T = P^T o (dP^T - delta_q) into shared memory (BF16, 128B swizzle)
+//              for the dK and dQ MMAs; finally writes dK and dV.
+//   warps 4-7  dQ warpgroup: thread = query row; reads each dQ tile from TMEM and
+//              adds it into the FP32 dQ accumulator in global memory.
+//   warp  8    MMA issuer;  warp 9  TMA producer.
+// Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_host.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kBlock = 128;     // keys per CTA tile and queries per step
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kStages = 2;      // query-tile ring depth (Q and dO)
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = kBlock * D * 2;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kQOff = kVOff + kTileBytes;
+  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
+  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;     // dS^T, 128 x 128 BF16
+  static constexpr int kBarOff = kDSOff + kBlock * kBlock * 2;
+  static constexpr int kSmemBytes = kBarOff + 512;
+  static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 128, kTmemDK = 256, kTmemDV = 256 + D;
+  static constexpr uint32_t kIdescSq = idesc_bf16(128, kBlock, false, false);  // S^T, dP^T
+  static constexpr uint32_t kIdescKV = idesc_bf16(128, D, false, true);        // dV (TMEM A), dK
+  static constexpr uint32_t kIdescQ = idesc_bf16(128, D, true, true);          // dQ: A = dS (MN-major)
+};
+
+struct Bars {
+  uint64_t kv_full;
+  uint64_t q_full[kStages], q_empty[kStages], do_full[kStages], do_empty[kStages];
+  uint64_t s_full, p_ready, dp_full, ds_ready, ds_empty, dq_full, dq_empty, mma_done;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+struct Params {
+  const float* lse;
+  const float* delta;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  uint32_t* status;
+  int N;
+  int BH;
+  int n_tiles;      // ceil(N / 128)
+  int causal;
+  float scale;
+  float scale_log2;
+};
+
+// --------------------------------------------------------------------------- preprocess
+// delta = rowsum(dO o O) in FP32 and dQ_acc = 0.  d/8 lanes per row, 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ dO,
+                                                         float* __restrict__ delta, float* __restrict__ delta_out,
+                                                         float* __restrict__ dq_acc, long long rows) {
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const int lane = threadIdx.x % 32;
+  const long long warp_global = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const long long row = warp_global * kRowsPerWarp + lane / kLanesPerRow;
+  const int c = (lane % kLanesPerRow) * 8;
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + c);
+    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + c);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 fa2 = __bfloat1622float2(pa[i]);
+      const float2 fb2 = __bfloat1622float2(pb[i]);
+      acc = fmaf(fa2.x, fb2.x, acc);
+      acc = fmaf(fa2.y, fb2.y, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + row * D + c);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int off = kLanesPerRow / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && (lane % kLanesPerRow) == 0) {
+    delta[row] = acc;
+    if (delta_out) delta_out[row] = acc;
+  }
+}
+
+// --------------------------------------------------------------------------- dQ convert
+__global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict__ dq_acc,
+                                                         __nv_bfloat16* __restrict__ dq, float scale,
+                                                         long long n8) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  uint4 out;
+  out.x = pack_bf16x2(a.x * scale, a.y * scale);
+  out.y = pack_bf16x2(a.z * scale, a.w * scale);
+  out.z = pack_bf16x2(b.x * scale, b.y * scale);
+  out.w = pack_bf16x2(b.z * scale, b.w * scale);
+  reinterpret_cast<uint4*>(dq)[i] = out;
+}
+
+// --------------------------------------------------------------------------- main kernel
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // The swizzled operand layouts need a 1024-byte aligned base; there is no slack
+  // for re-alignment at d = 128, so refuse to run rather than compute garbage.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, kDevBounds);
+    return;
+  }
+  Bars& sh = *reinterpret_cast<Bars*>(smem + C::kBarOff);
+  volatile uint32_t* abort_flag = &sh.abort_flag;
+  const int warp = threadIdx.x / 32;
+  const int jt = blockIdx.x / p.BH;  // key tile (ascending: heaviest first when causal)
+  const int bh = blockIdx.x % p.BH;
+  const int i0 = p.causal ? jt : 0;  // first query tile that sees this key tile
+  const int n_it = p.n_tiles - i0;
+
+  if (threadIdx.x == 0) {
+    sh.abort_flag = 0;
+    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh.q_full[s], 1);
+      mbar_init(&sh.q_empty[s], 1);
+      mbar_init(&sh.do_full[s], 1);
+      mbar_init(&sh.do_empty[s], 1);
+    }
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.p_ready, kBlock);
+    mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.ds_ready, kBlock);
+    mbar_init(&sh.ds_empty, 1);
+    mbar_init(&sh.dq_full, 1);
+    mbar_init(&sh.dq_empty, kBlock);
+    mbar_init(&sh.mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmDO);
+      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kTileBytes);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(smem + C::kKOff + c * 16384, &tmK, &sh.kv_full, c * 64, jt * kBlock, bh);
+        tma_load_3d(smem + C::kVOff + c * 16384, &tmV, &sh.kv_full, c * 64, jt * kBlock, bh);
+      }
+      int nq = 0, ndo = 0;
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        const int row0 = (i0 + it) * kBlock;
+        if (!mbar_wait(&sh.q_empty[s], ph ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sh.q_full[s], C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::kQOff + s * C::kTileBytes + c * 16384, &tmQ, &sh.q_full[s], c * 64, row0, bh);
+        nq = it + 1;
+        if (!mbar_wait(&sh.do_empty[s], ph ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sh.do_full[s], C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::kDOOff + s * C::kTileBytes + c * 16384, &tmDO, &sh.do_full[s], c * 64, row0, bh);
+        ndo = it + 1;
+      }
+      if (*abort_flag) {
+        // let copies still in flight land before the CTA's shared memory goes away
+        volatile uint32_t ignore_abort = 0;
+        mbar_wait(&sh.kv_full, 0, &ignore_abort, p.status);
+        for (int it = max(0, nq - kStages); it < nq; ++it)
+          mbar_wait(&sh.q_full[it % kStages], (it / kStages) & 1, &ignore_abort, p.status);
+        for (int it = max(0, ndo - kStages); it < ndo; ++it)
+          mbar_wait(&sh.do_full[it % kStages], (it / kStages) & 1, &ignore_abort, p.status);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      const uint32_t sK = smem_u32(smem + C::kKOff), sV = smem_u32(smem + C::kVOff);
+      const uint32_t sQ = smem_u32(smem + C::kQOff), sDO = smem_u32(smem + C::kDOOff);
+      const uint32_t sDS = smem_u32(smem + C::kDSOff);
+      // K-major operand with D (or 128) columns: 16 KB per 64 columns, 32 B per k-step
+      auto kmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024); };
+      // MN-major operand with 128 K rows: 2 KB per k-step, 16 KB between 64-column blocks
+      auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, 16384, 1024); };
+      bool ok = mbar_wait(&sh.kv_full, 0, abort_flag, p.status);
+      auto issue_s = [&](int it) {  // S^T = K_j Q_i^T
+        const int s = it % kStages;
+        if (!(ok = mbar_wait(&sh.q_full[s], (it / kStages) & 1, abort_flag, p.status))) return;
+        tc_fence_after();
+        const uint32_t q = sQ + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kTmemS, kmaj(sK, kk), kmaj(q, kk), C::kIdescSq, kk > 0);
+        tc_commit(&sh.s_full);
+      };
+      if (ok && n_it > 0) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        const uint32_t q = sQ + s * C::kTileBytes, dO = sDO + s * C::kTileBytes;
+        // dP^T = V_j dO_i^T   (its columns hold the previous dQ tile: wait until drained)
+        if (!(ok = mbar_wait(&sh.do_full[s], ph, abort_flag, p.status))) break;
+        if (it > 0 && !(ok = mbar_wait(&sh.dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kTmemDP, kmaj(sV, kk), kmaj(dO, kk), C::kIdescSq, kk > 0);
+        tc_commit(&sh.dp_full);
+        // dV += P^T dO_i   (P^T from TMEM, 8 columns per k-step of 16 queries)
+        if (!(ok = mbar_wait(&sh.p_ready, it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk)
+          mma_ts(tmem + C::kTmemDV, tmem + C::kTmemS + kk * 8, mnmaj(dO, kk), C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&sh.do_empty[s]);
+        // next S^T (overwrites P^T only after the dV MMA above has read it: same-thread MMAs run in order)
+        if (it + 1 < n_it) {
+          issue_s(it + 1);
+          if (!ok) break;
+        }
+        // dK += dS^T Q_i ;  dQ_i = dS K_j
+        if (!(ok = mbar_wait(&sh.ds_ready, it & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk)
+          mma_ss(tmem + C::kTmemDK, kmaj(sDS, kk), mnmaj(q, kk), C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk)
+          mma_ss(tmem + C::kTmemDQ, mnmaj(sDS, kk), mnmaj(sK, kk), C::kIdescQ, kk > 0);
+        tc_commit(&sh.q_empty[s]);
+        tc_commit(&sh.ds_empty);
+        tc_commit(&sh.dq_full);
+      }
+      tc_commit(&sh.mma_done);
+      mbar_wait(&sh.mma_done, 0, abort_flag, p.status);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------------ P^T / dS^T warpgroup
+    const int lane_base = warp * 32;
+    const int r = lane_base + (threadIdx.x % 32);  // key row within the tile
+    const int key = jt * kBlock + r;
+    const uint32_t tS = tmem + C::kTmemS + ((uint32_t)lane_base << 16);
+    const uint32_t tDP = tmem + C::kTmemDP + ((uint32_t)lane_base << 16);
+    const float c = p.scale_log2;
+    const float* lse = p.lse + (size_t)bh * p.N;
+    const float* dl = p.delta + (size_t)bh * p.N;
+    uint8_t* ds_row = smem + C::kDSOff + r * 128;
+    const uint32_t sw = (uint32_t)(r & 7);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int q0 = (i0 + it) * kBlock;
+      // visible queries of this key row: q >= key when causal, q < N always
+      const int qlo = p.causal ? key - q0 : 0;   // first visible column
+      const int qhi = p.N - q0;                  // one past the last visible column
+      if (!(ok = mbar_wait(&sh.s_full, it & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      float pr[kBlock];
+#pragma unroll
+      for (int c0 = 0; c0 < kBlock; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(tS + c0, w);
+        tmem_ld_wait();
+        reg_fence(w);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const int qc = c0 + i;
+          float lv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) lv[u] = (q0 + qc + u < p.N) ? __ldg(lse + q0 + qc + u) : 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const bool vis = (qc + u >= qlo) && (qc + u < qhi) && (key < p.N);
+            const float e = ex2_approx(fmaf(__uint_as_float(w[i + u]), c, -lv[u] * 1.4426950408889634f));
+            pr[qc + u] = vis ? e : 0.f;
+          }
+        }
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[h * 64 + 2 * i], pr[h * 64 + 2 * i + 1]);
+          tmem_st32(tS + h * 32, pk);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sh.p_ready);
+      // dS^T = P^T o (dP^T - delta_q), written 32 queries at a time into the swizzled
+      // dS^T tile once the previous step's dK / dQ MMAs have finished reading it
+      if (!(ok = mbar_wait(&sh.dp_full, it & 1, abort_flag, p.status))) break;
+      if (it > 0 && !(ok = mbar_wait(&sh.ds_empty, (it - 1) & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < kBlock; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(tDP + c0, w);
+        tmem_ld_wait();
+        reg_fence(w);
+        uint32_t dsk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const int qc = c0 + i;
+          float d4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) d4[u] = (q0 + qc + u < p.N) ? __ldg(dl + q0 + qc + u) : 0.f;
+          dsk[i / 2] = pack_bf16x2(pr[qc] * (__uint_as_float(w[i]) - d4[0]),
+                                   pr[qc + 1] * (__uint_as_float(w[i + 1]) - d4[1]));
+          dsk[i / 2 + 1] = pack_bf16x2(pr[qc + 2] * (__uint_as_float(w[i + 2]) - d4[2]),
+                                       pr[qc + 3] * (__uint_as_float(w[i + 3]) - d4[3]));
+        }
+        // row r of dS^T, 16-byte chunk g (8 queries) -> block g/8, swizzled chunk (g%8) ^ (r%8)
+#pragma unroll
+        for (int gg = 0; gg < 4; ++gg) {
+          const int g = c0 / 8 + gg;
+          *reinterpret_cast<uint4*>(ds_row + (g / 8) * 16384 + ((((uint32_t)g % 8) ^ sw) << 4)) =
+              make_uint4(dsk[4 * gg], dsk[4 * gg + 1], dsk[4 * gg + 2], dsk[4 * gg + 3]);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(&sh.ds_ready);
+    }
+    // ------------------------------------------------------------------ dK, dV epilogue
+    if (ok && n_it > 0 && mbar_wait(&sh.mma_done, 0, abort_flag, p.status)) {
+      tc_fence_after();
+      const bool valid = key < p.N;
+      const size_t orow = ((size_t)bh * p.N + (valid ? key : 0)) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t t = tmem + (which == 0 ? C::kTmemDK : C::kTmemDV) + ((uint32_t)lane_base << 16);
+        const float mul = which == 0 ? p.scale : 1.f;
+        __nv_bfloat16* out = which == 0 ? p.dk : p.dv;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t w[32];
+          tmem_ld32(t + c0, w);
+          tmem_ld_wait();
+          reg_fence(w);
+          uint4 pkd[4];
+          uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + orow + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+          }
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ dQ warpgroup
+    const int lane_base = (warp - 4) * 32;
+    const int r = lane_base + (threadIdx.x % 32);  // query row within the current query tile
+    const uint32_t tDQ = tmem + C::kTmemDQ + ((uint32_t)lane_base << 16);
+    for (int it = 0; it < n_it; ++it) {
+      if (!mbar_wait(&sh.dq_full, it & 1, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int qrow = (i0 + it) * kBlock + r;
+      float* dst = p.dq_acc + ((size_t)bh * p.N + (qrow < p.N ? qrow : 0)) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(tDQ + c0, w);
+        tmem_ld_wait();
+        reg_fence(w);
+        if (qrow < p.N) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            atomicAdd(reinterpret_cast<float4*>(dst + c0 + i),
+                      make_float4(__uint_as_float(w[i]), __uint_as_float(w[i + 1]), __uint_as_float(w[i + 2]),
+                                  __uint_as_float(w[i + 3])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.dq_empty);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace bwd
+}  // namespace fa
+
+namespace {
+
+template <int D>
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
+               void* dk, void* dv, float* delta_out, int B, int H, int N, int causal, float scale, float* dq_acc,
+               float* delta, cudaStream_t stream) {
+  using namespace fa;
+  using C = bwd::Cfg<D>;
+  const long long rows = (long long)B * H * N;
+  int rc;
+  {
+    constexpr int rows_per_block = 8 * (32 / (D / 8));
+    const long long grid = (rows + rows_per_block - 1) / rows_per_block;
+    bwd::fa_bwd_preprocess<D><<<(unsigned)grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
+                                                                static_cast<const __nv_bfloat16*>(dO), delta,
+                                                                delta_out, dq_acc, rows);
+    if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_preprocess"))) return rc;
+  }
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = make_tmap_bhnd(&tq, q, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tk, k, B * H, N, D, bwd::kBlock)) ||
+      (rc = make_tmap_bhnd(&tv, v, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tdo, dO, B * H, N, D, bwd::kBlock)))
+    return rc;
+  bwd::Params p{};
+  p.lse = lse;
+  p.delta = delta;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.status = device_status_word();
+  if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
+  p.N = N;
+  p.BH = B * H;
+  p.n_tiles = (N + bwd::kBlock - 1) / bwd::kBlock;
+  p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  auto kern = bwd::fa_bwd_main<D>;
+  if ((rc = check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
+                       "cudaFuncSetAttribute(bwd)")))
+    return rc;
+  kern<<<(unsigned)(p.n_tiles * p.BH), bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_main"))) return rc;
+  const long long n8 = rows * D / 8;
+  bwd::fa_bwd_dq_convert<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
+                                                                           scale, n8);
+  return check_cuda(cudaGetLastError(), "launch fa_bwd_dq_convert");
+}
+
+}  // namespace
+
+extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (fa::check_shape(B, H, N, d)) return 0;
+  const size_t bhn = (size_t)B * H * N;
+  return fa::round_up(bhn * d * 4, 256) + fa::round_up(bhn * 4, 256);
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                      void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N, int d, int causal,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  using namespace fa;
+  clear_error();
+  int rc;
+  if ((rc = check_shape(B, H, N, d))) return rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) || (rc = check_ptr(o, "o")) ||
+      (rc = check_ptr(lse, "lse")) || (rc = check_ptr(dO, "dO")) || (rc = check_ptr(dq, "dq")) ||
+      (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
+    return rc;
+  if (delta_out && (reinterpret_cast<uintptr_t>(delta_out) & 3))
+    return set_error(FA_ERR_INVALID_ARG, "delta_out is not 4-byte aligned");
+  if (!(scale > 0.f) || !isfinite(scale)) return set_error(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return set_error(FA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
+  if (workspace_bytes < need)
+    return set_error(FA_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  const size_t bhn = (size_t)B * H * N;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(bhn * d * 4, 256));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, dq_acc,
+                                  delta, s)
+                 : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale,
+                                   dq_acc, delta, s);
+}

@@ -1,0 +1,127 @@
+// Host-side common code: thread-local error messages, the per-device status
+// word, tensor-map encoding through the driver entry point, fa_device_status.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "fa_host.h"
+#include "sm103.cuh"
+
+namespace fa {
+
+static thread_local char g_last_error[512] = "";
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+void clear_error() { g_last_error[0] = '\0'; }
+
+int check_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return FA_OK;
+  return set_error(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_status[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+}  // namespace
+
+uint32_t* device_status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status[dev]) {
+    uint32_t* p = nullptr;
+    if (cudaMalloc(&p, sizeof(uint32_t)) != cudaSuccess) return nullptr;
+    if (cudaMemset(p, 0, sizeof(uint32_t)) != cudaSuccess) return nullptr;
+    g_status[dev] = p;
+  }
+  return g_status[dev];
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = n > 0 ? n : 148;
+  }
+  return g_sms[dev];
+}
+
+int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return set_error(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return FA_OK;
+}
+
+int check_shape(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return set_error(FA_ERR_INVALID_ARG, "B, H, N must be >= 1 (got %d, %d, %d)", B, H, N);
+  if ((long long)B * H * N >= (1ll << 31))
+    return set_error(FA_ERR_INVALID_ARG, "B*H*N must be < 2^31");
+  if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
+  return FA_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+  if (!p) return set_error(FA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(p) & 15) return set_error(FA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return FA_OK;
+}
+
+}  // namespace fa
+
+extern "C" int fa_device_status(void* stream) {
+  uint32_t* w = fa::device_status_word();
+  if (!w) return fa::set_error(FA_ERR_CUDA, "status word unavailable");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc = fa::check_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  if (rc) return rc;
+  uint32_t v = 0;
+  rc = fa::check_cuda(cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost), "read status word");
+  if (rc) return rc;
+  if (v) {
+    rc = fa::check_cuda(cudaMemset(w, 0, sizeof(uint32_t)), "clear status word");
+    if (rc) return rc;
+  }
+  if (v & fa::kDevTimeout) return fa::set_error(FA_ERR_TIMEOUT, "a kernel's bounded wait timed out");
+  if (v & fa::kDevBounds) return fa::set_error(FA_ERR_DEVICE_BOUNDS, "a device bounds check failed");
+  return FA_OK;
+}
+
+extern "C" const char* fa_last_error(void) { return fa::g_last_error; }
+
+extern "C" const char* fa_version(void) { return "numerics_tcgen05_tmem_gb300 0.1 (sm_103a)"; }

@@ -1,0 +1,452 @@
+// Attention forward for sm_103a: tcgen05 MMAs into tensor memory, TMA-fed
+// K/V ring, per-row online softmax with the stabilised shift.
+//
+// Method (ijyty.com/news/896914, §2.1): for each key block j of a query tile,
+//   S = Q K_j^T (raw, FP32),  m = shift(running stats),  P~ = exp(scale (S - m)),
+//   l = exp(scale (m_prev - m)) l + rowsum(P~),
+//   O = exp(scale (m_prev - m)) O + P~ V_j,   finally O = O / l,
+//   lse = scale m + ln l.
+// Stabilised shift (same page, §4.1/§4.2; web578.cn "mechanism 2"): each row
+// keeps its running raw maximum rm and how often it occurred, rs; the shift is
+//   m = beta rm if rm > 0 and rs > 1;  m = 0 if rm < 0 and rs > 1;  else m = rm,
+// evaluated with selects (no divergent branch) after every block.
+// Precision (jsqmd.com "Flash Attention低精度训练稳定性优化实践" §3.2): QK^T and
+// P~V accumulate in FP32 (TMEM), the softmax runs in FP32, P~ is rounded to BF16
+// (round-to-nearest-even) for the P~V product.
+//
+// CTA organisation (one CTA = two 128-row query tiles of one (b, h)):
+//   warps 0-3  softmax warpgroup for tile 0 (thread = one query row = one TMEM lane)
+//   warps 4-7  softmax warpgroup for tile 1
+//   warp  8    MMA issuer (one elected thread)
+//   warp  9    TMA producer (one elected thread)
+// Tensor memory (512 columns): S0 | S1 | O0 | O1; the BF16 P~ of a tile is written
+// over the first 64 columns of its S (each thread has read its own S row first)
+// and fed to the P~V MMA straight from TMEM.
+#include <cuda_bf16.h>
+#include <math.h>
+#include <stdio.h>
+
+#include "fa_host.h"
+#include "sm103.cuh"
+
+namespace fa {
+namespace fwd {
+
+constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
+constexpr int kBlockN = 128;   // keys per block
+constexpr int kTiles = 2;      // query tiles per CTA
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+
+template <int D>
+struct Cfg {
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kTileBytes = kBlockM * D * 2;   // one 128 x D BF16 tile (Q, K or V)
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kTiles * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kVOff + kStages * kTileBytes + 1024;  // +1024 for alignment
+  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + D;
+  static constexpr uint32_t kIdescS = idesc_bf16(128, kBlockN, false, false);  // Q K^T, both K-major
+  static constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);         // P~ (TMEM) x V (MN-major)
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  float* stat_rm;
+  int32_t* stat_rs;
+  int8_t* stat_branch;
+  int32_t* stat_ones;
+  uint32_t* status;
+  int N;
+  int BH;
+  int n_qblocks;   // ceil(N / 256)
+  int causal;
+  float scale;
+  float scale_log2;  // scale * log2(e)
+  float beta;
+};
+
+struct Shared {
+  uint64_t q_full;
+  uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
+  uint64_t s_full[kTiles], p_ready[kTiles], pv_done[kTiles];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+// Which key blocks tile t of query block qb attends: [0, nb).  0 if the tile is
+// entirely past N.
+__device__ __forceinline__ int tile_blocks(const Params& p, int qb, int t) {
+  const int row0 = qb * (kTiles * kBlockM) + t * kBlockM;
+  if (row0 >= p.N) return 0;
+  const int nk = (p.N + kBlockN - 1) / kBlockN;
+  if (!p.causal) return nk;
+  const int last = (row0 + kBlockM - 1) / kBlockN;  // diagonal block of the tile
+  return min(nk, last + 1);
+}
+
+// Load 32 consecutive FP32 columns of this thread's TMEM lane into v[off..off+31].
+__device__ __forceinline__ void ld_row32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+  reg_fence(r);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int D, bool kStable, bool kStats>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Shared sh;
+  volatile uint32_t* abort_flag = &sh.abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  // heaviest (largest causal) query blocks first
+  const int qb = p.causal ? (p.n_qblocks - 1 - (int)(blockIdx.x / p.BH)) : (int)(blockIdx.x / p.BH);
+  const int bh = blockIdx.x % p.BH;
+  const int nb0 = tile_blocks(p, qb, 0), nb1 = tile_blocks(p, qb, 1);
+  const int nbmax = max(nb0, nb1);
+
+  if (threadIdx.x == 0) {
+    sh.abort_flag = 0;
+    mbar_init(&sh.q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&sh.k_full[s], 1);
+      mbar_init(&sh.k_empty[s], 1);
+      mbar_init(&sh.v_full[s], 1);
+      mbar_init(&sh.v_empty[s], 1);
+    }
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&sh.s_full[t], 1);
+      mbar_init(&sh.p_ready[t], kBlockM);
+      mbar_init(&sh.pv_done[t], 1);
+    }
+    mbar_init(&sh.mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ TMA producer
+    if (elect_one()) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const int ntiles = (nb1 > 0) ? 2 : 1;
+      mbar_arrive_expect_tx(&sh.q_full, ntiles * C::kTileBytes);
+      for (int t = 0; t < ntiles; ++t)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * 16384, &tmQ, &sh.q_full, c * 64,
+                      qb * (kTiles * kBlockM) + t * kBlockM, bh);
+      int nk_issued = 0, nv_issued = 0;
+      for (int j = 0; j < nbmax; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!mbar_wait(&sh.k_empty[s], ph ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sh.k_full[s], C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * 16384, &tmK, &sh.k_full[s], c * 64, j * kBlockN, bh);
+        nk_issued = j + 1;
+        if (!mbar_wait(&sh.v_empty[s], ph ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sh.v_full[s], C::kTileBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + c * 16384, &tmV, &sh.v_full[s], c * 64, j * kBlockN, bh);
+        nv_issued = j + 1;
+      }
+      if (*abort_flag) {
+        // let copies still in flight land before the CTA's shared memory goes away
+        volatile uint32_t ignore_abort = 0;
+        mbar_wait(&sh.q_full, 0, &ignore_abort, p.status);
+        for (int j = max(0, nk_issued - C::kStages); j < nk_issued; ++j)
+          mbar_wait(&sh.k_full[j % C::kStages], (j / C::kStages) & 1, &ignore_abort, p.status);
+        for (int j = max(0, nv_issued - C::kStages); j < nv_issued; ++j)
+          mbar_wait(&sh.v_full[j % C::kStages], (j / C::kStages) & 1, &ignore_abort, p.status);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      const uint32_t sQ = smem_u32(smem + C::kQOff);
+      const uint32_t sK = smem_u32(smem + C::kKOff);
+      const uint32_t sV = smem_u32(smem + C::kVOff);
+      const int nb[2] = {nb0, nb1};
+      bool ok = mbar_wait(&sh.q_full, 0, abort_flag, p.status);
+      tc_fence_after();
+      // S_t = Q_t K_j^T over D/16 k-steps (K-major SW128 operands, 16 KB per 64 columns)
+      auto issue_s = [&](int t, int s) {
+        const uint32_t a0 = sQ + t * C::kTileBytes, b0 = sK + s * C::kTileBytes;
+        const uint32_t d = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::kIdescS, kk > 0);
+        }
+        tc_commit(&sh.s_full[t]);
+      };
+      // O_t += P~_t V_j: P~ from TMEM (K = 128 keys, 8 columns per k-step), V MN-major
+      auto issue_pv = [&](int t, int s, int j) {
+        const uint32_t b0 = sV + s * C::kTileBytes;
+        const uint32_t d = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1);
+        const uint32_t a = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          mma_ts(d, a + kk * 8, sdesc_sw128(b0 + kk * 2048, 16384, 1024), C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&sh.pv_done[t]);
+      };
+      // Order: S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 PV1_1 S1_2 | ... | PV0_last PV1_last
+      for (int j = 0; ok && j <= nbmax; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        const int sp = (j + C::kStages - 1) % C::kStages;  // stage of block j-1
+        if (j < nbmax) {
+          if (!(ok = mbar_wait(&sh.k_full[s], ph, abort_flag, p.status))) break;
+          tc_fence_after();
+        }
+        if (j > 0) {
+          if (!(ok = mbar_wait(&sh.v_full[sp], ((j - 1) / C::kStages) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+        }
+        for (int t = 0; t < kTiles; ++t) {
+          if (j > 0 && j - 1 < nb[t]) {
+            if (!(ok = mbar_wait(&sh.p_ready[t], (j - 1) & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_pv(t, sp, j - 1);
+          }
+          if (j < nb[t]) issue_s(t, s);
+        }
+        if (!ok) break;
+        if (j < nbmax) tc_commit(&sh.k_empty[s]);
+        if (j > 0) tc_commit(&sh.v_empty[sp]);
+      }
+      // every MMA issued above has completed before TMEM is released
+      tc_commit(&sh.mma_done);
+      mbar_wait(&sh.mma_done, 0, abort_flag, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp / 4;                      // tile
+    const int lane_base = (warp % 4) * 32;       // TMEM lane quarter of this warp
+    const int r = lane_base + (threadIdx.x % 32);  // row within the tile
+    const int nb = (t == 0) ? nb0 : nb1;
+    const int row = qb * (kTiles * kBlockM) + t * kBlockM + r;
+    const uint32_t tS = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1) + ((uint32_t)lane_base << 16);
+    const uint32_t tO = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1) + ((uint32_t)lane_base << 16);
+    const float c = p.scale_log2;
+    float rm = -INFINITY, m = -INFINITY, l = 0.f;
+    int rs = 0, ones = 0;
+    int branch = 0;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      if (!(ok = mbar_wait(&sh.s_full[t], j & 1, abort_flag, p.status))) break;
+      tc_fence_after();
+      float sv[kBlockN];
+#pragma unroll
+      for (int c0 = 0; c0 < kBlockN; c0 += 32) ld_row32(tS + c0, sv + c0);
+      // mask: keys past N, and keys after the query on the causal diagonal
+      const int col0 = j * kBlockN;
+      const int lim = p.causal ? min(p.N - col0, row - col0 + 1) : (p.N - col0);
+      if (lim < kBlockN) {
+#pragma unroll
+        for (int i = 0; i < kBlockN; ++i) sv[i] = (i < lim) ? sv[i] : -INFINITY;
+      }
+      float bm = sv[0];
+#pragma unroll
+      for (int i = 1; i < kBlockN; ++i) bm = fmaxf(bm, sv[i]);
+      float m_new;
+      if constexpr (kStable || kStats) {
+        // running (max, count) merge: rs' = [rm == rm'] rs + [bm == rm'] bc
+        int bc = 0;
+#pragma unroll
+        for (int i = 0; i < kBlockN; ++i) bc += (sv[i] == bm) ? 1 : 0;
+        bc = (bm == -INFINITY) ? 0 : bc;
+        const float rm_new = fmaxf(rm, bm);
+        rs = ((rm == rm_new) ? rs : 0) + ((bm == rm_new) ? bc : 0);
+        rm = rm_new;
+      } else {
+        rm = fmaxf(rm, bm);
+      }
+      if constexpr (kStable) {
+        const bool rep = rs > 1;
+        const bool pos = rep && (rm > 0.f), neg = rep && (rm < 0.f);
+        m_new = pos ? p.beta * rm : (neg ? 0.f : rm);
+        branch = pos ? 1 : (neg ? 2 : 0);
+      } else {
+        m_new = rm;
+      }
+      const float alpha = ex2_approx((m - m_new) * c);  // 0 on the first block (m = -inf)
+      const float nmc = -m_new * c;
+      uint32_t pk[kBlockN / 2];
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < kBlockN; i += 2) {
+        const float p0 = ex2_approx(fmaf(sv[i], c, nmc));
+        const float p1 = ex2_approx(fmaf(sv[i + 1], c, nmc));
+        sum0 += p0;
+        sum1 += p1;
+        pk[i / 2] = pack_bf16x2(p0, p1);
+      }
+      if constexpr (kStats) {
+#pragma unroll
+        for (int i = 0; i < kBlockN / 2; ++i)
+          ones += ((pk[i] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((pk[i] >> 16) == 0x3F80u ? 1 : 0);
+      }
+      l = fmaf(alpha, l, sum0 + sum1);
+      __syncwarp();
+      {
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = pk[h * 32 + i];
+          tmem_st32(tS + h * 32, w);
+        }
+      }
+      tmem_st_wait();
+      // rescale O by alpha once the previous P~V has landed (skip when the whole warp has alpha == 1)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!(ok = mbar_wait(&sh.pv_done[t], (j - 1) & 1, abort_flag, p.status))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t w[32];
+          tmem_ld32(tO + c0, w);
+          tmem_ld_wait();
+          reg_fence(w);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+          tmem_st32(tO + c0, w);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.p_ready[t]);
+      m = m_new;
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && nb > 0 && mbar_wait(&sh.pv_done[t], (nb - 1) & 1, abort_flag, p.status)) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool valid = row < p.N;
+      const size_t orow = ((size_t)bh * p.N + (valid ? row : 0)) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(tO + c0, w);
+        tmem_ld_wait();
+        reg_fence(w);
+        uint4 pkd[4];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pw[i] = pack_bf16x2(__uint_as_float(w[2 * i]) * inv_l, __uint_as_float(w[2 * i + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + orow + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
+        }
+      }
+      if (valid) {
+        const size_t srow = (size_t)bh * p.N + row;
+        p.lse[srow] = m * p.scale + logf(l);
+        if constexpr (kStats) {
+          if (p.stat_rm) p.stat_rm[srow] = rm;
+          if (p.stat_rs) p.stat_rs[srow] = rs;
+          if (p.stat_branch) p.stat_branch[srow] = (int8_t)branch;
+          if (p.stat_ones) p.stat_ones[srow] = ones;
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fwd
+}  // namespace fa
+
+namespace {
+
+template <int D, bool kStable, bool kStats>
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::fwd::Params& p,
+               cudaStream_t stream) {
+  using C = fa::fwd::Cfg<D>;
+  auto kern = fa::fwd::fa_fwd_kernel<D, kStable, kStats>;
+  int rc = fa::check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
+                          "cudaFuncSetAttribute(fwd)");
+  if (rc) return rc;
+  const dim3 grid((unsigned)(p.n_qblocks * p.BH));
+  kern<<<grid, fa::fwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  return fa::check_cuda(cudaGetLastError(), "launch fa_fwd_kernel");
+}
+
+template <int D>
+int dispatch_fwd(bool stable, bool stats, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                 const fa::fwd::Params& p, cudaStream_t s) {
+  if (stable) return stats ? launch_fwd<D, true, true>(tq, tk, tv, p, s) : launch_fwd<D, true, false>(tq, tk, tv, p, s);
+  return stats ? launch_fwd<D, false, true>(tq, tk, tv, p, s) : launch_fwd<D, false, false>(tq, tk, tv, p, s);
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                      int causal, float scale, int stable, float beta, const fa_row_stats* stats, void* stream) {
+  using namespace fa;
+  clear_error();
+  int rc;
+  if ((rc = check_shape(B, H, N, d))) return rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) || (rc = check_ptr(o, "o")))
+    return rc;
+  if (!lse) return set_error(FA_ERR_INVALID_ARG, "lse is NULL");
+  if (!(scale > 0.f) || !isfinite(scale)) return set_error(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (stable != 0 && stable != 1) return set_error(FA_ERR_INVALID_ARG, "stable must be 0 or 1 (got %d)", stable);
+  if (stable && (!isfinite(beta) || beta < 1.f)) return set_error(FA_ERR_INVALID_ARG, "beta must be finite and >= 1");
+  fwd::Params p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  bool want_stats = false;
+  if (stats) {
+    p.stat_rm = stats->row_max_raw;
+    p.stat_rs = stats->row_ties;
+    p.stat_branch = stats->row_branch;
+    p.stat_ones = stats->row_ones;
+    want_stats = p.stat_rm || p.stat_rs || p.stat_branch || p.stat_ones;
+  }
+  p.status = device_status_word();
+  if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
+  p.N = N;
+  p.BH = B * H;
+  p.n_qblocks = (N + fwd::kTiles * fwd::kBlockM - 1) / (fwd::kTiles * fwd::kBlockM);
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.beta = beta;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_tmap_bhnd(&tq, q, B * H, N, d, fwd::kBlockM)) || (rc = make_tmap_bhnd(&tk, k, B * H, N, d, fwd::kBlockN)) ||
+      (rc = make_tmap_bhnd(&tv, v, B * H, N, d, fwd::kBlockN)))
+    return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? dispatch_fwd<64>(stable != 0, want_stats, tq, tk, tv, p, s)
+                 : dispatch_fwd<128>(stable != 0, want_stats, tq, tk, tv, p, s);
+}

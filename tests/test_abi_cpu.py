@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads without a GPU and exports what include/fa.h declares.
+
+Only host-side logic runs here (argument validation, workspace sizing); no
+kernel is launched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from numerics_tcgen05_tmem_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    assert set(binding.EXPORTS) <= set(names), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+
+
+def test_version_string(lib):
+    assert b"sm_103a" in lib.fa_version()
+
+
+def test_workspace_size(lib):
+    B, H, N, d = 2, 3, 1000, 128
+    want = -(-(B * H * N * d * 4) // 256) * 256 + -(-(B * H * N * 4) // 256) * 256
+    assert lib.fa_bwd_workspace_size(B, H, N, d) == want
+    assert lib.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+    assert lib.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+
+
+def _fwd(lib, q=None, k=None, v=None, o=None, lse=None, B=1, H=1, N=128, d=64, causal=1, scale=0.125,
+         stable=1, beta=1.25):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, causal, scale, stable, beta, None, None)
+
+
+def test_invalid_arguments_fail_before_touching_the_gpu(lib):
+    good = ctypes.c_void_p(1 << 20)     # aligned, never dereferenced: validation fails first
+    assert _fwd(lib, None, good, good, good, good) == binding.FA_ERR_INVALID_ARG
+    assert b"q is NULL" in lib.fa_last_error()
+    assert _fwd(lib, ctypes.c_void_p((1 << 20) + 8), good, good, good, good) == binding.FA_ERR_INVALID_ARG
+    assert b"aligned" in lib.fa_last_error()
+    assert _fwd(lib, good, good, good, good, good, d=96) == binding.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, good, good, good, good, good, N=0) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, None) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, good, scale=float("nan")) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, good, scale=0.0) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, good, stable=2) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, good, beta=0.9) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, good, beta=float("inf")) == binding.FA_ERR_INVALID_ARG
+
+
+def test_backward_invalid_arguments(lib):
+    good = ctypes.c_void_p(1 << 20)
+    ws = lib.fa_bwd_workspace_size(1, 1, 128, 64)
+    rc = lib.fa_bwd(good, good, good, good, good, good, good, good, None, None, 1, 1, 128, 64, 1, 0.125,
+                    good, ws, None)
+    assert rc == binding.FA_ERR_INVALID_ARG
+    rc = lib.fa_bwd(good, good, good, good, good, good, good, good, good, None, 1, 1, 128, 64, 1, 0.125,
+                    good, ws - 256, None)
+    assert rc == binding.FA_ERR_INVALID_ARG
+    assert b"workspace" in lib.fa_last_error()
