@@ -1,0 +1,380 @@
+#!/usr/bin/env python
+"""Benchmark of the attention forward + backward hot path on one GB300.
+
+One step = fa_fwd (stabilised shift, beta = 1.25) followed by the three
+backward stages (delta preprocess, recomputing main kernel, dQ convert) on the
+LLaMA-7B shaped causal problem B=1, H=32, N=8192, d=128, with inputs resident
+in HBM.  The metric is algorithmic TFLOP/s (forward 4 B H N^2 d / 2 for causal,
+backward 2.5x that), whole job, and its fraction of the measured dense BF16
+peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (numpy
+FP64) on the host cores instead, on a bounded sample of the same workload.
+Under torchrun with N > 1 every rank runs its own independent shard of
+(batch, head) problems of the same size (weak scaling, no collective on the
+data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd / bwd TFLOP/s (BF16, causal) and % of GB300 dense BF16 peak"
+WORKLOAD = {"name": "llama7b_long", "B": 1, "H": 32, "N": 8192, "d": 128, "causal": True, "stable": 1,
+            "beta": 1.25}
+
+
+def flops_fwd(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def flops_bwd(B, H, N, d, causal):
+    return 2.5 * flops_fwd(B, H, N, d, causal)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16_tflops": pk["bf16_tflops"], "bf16_tflops_sustained": pk.get("bf16_tflops_sustained"),
+                "hbm_gbs": pk["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle baseline
+def oracle_sample_run(heads=1):
+    """One oracle forward + backward of `heads` heads of the workload (numpy FP64 on the host)."""
+    from numerics_tcgen05_tmem_gb300 import inputs
+    from oracle import attention as A
+    w = inputs.llama7b_long(heads=list(range(heads)))
+    t0 = time.perf_counter()
+    f = A.forward(w.q, w.k, w.v, w.scale, True, stable=WORKLOAD["stable"], beta=WORKLOAD["beta"])
+    A.backward(w.q, w.k, w.v, f["o"], f["lse"], w.do, w.scale, True)
+    dt = time.perf_counter() - t0
+    fl = flops_fwd(1, heads, WORKLOAD["N"], WORKLOAD["d"], True) + flops_bwd(1, heads, WORKLOAD["N"], WORKLOAD["d"], True)
+    return fl, dt
+
+
+def cpu_cores():
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+def cpu_baseline():
+    fl, dt = oracle_sample_run(1)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "1 of 32 heads (N=8192, d=128, causal) forward + backward, numpy FP64; "
+                      f"{dt:.1f} s for {fl / 1e9:.0f} GFLOP"}
+
+
+# --------------------------------------------------------------------------- traffic from a committed ncu summary
+def kernel_sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "numerics_tcgen05_tmem_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag):
+    """DRAM bytes per launch recorded in profiles/ for this kernel, if taken on the current sources."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    sha = kernel_sources_sha()
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith(".md"):
+            continue
+        txt = open(os.path.join(pdir, fn)).read()
+        m = re.search(r"traffic_bytes_per_launch\[" + re.escape(kernel_tag) + r"\]:\s*([0-9.eE+]+)", txt)
+        s = re.search(r"kernel_sources_sha:\s*([0-9a-f]+)", txt)
+        if m and s and s.group(1) == sha:
+            return float(m.group(1))
+    return None
+
+
+# --------------------------------------------------------------------------- native arm
+def run_native(args):
+    import torch
+
+    from numerics_tcgen05_tmem_gb300 import binding, build, inputs
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    build.build()
+    binding.load()
+    dev = torch.device("cuda", local)
+    W = WORKLOAD
+    B, H, N, d, causal = W["B"], W["H"], W["N"], W["d"], W["causal"]
+    w = inputs.llama7b_long()
+    scale = w.scale
+    host = [t.pin_memory() for t in (w.q, w.k, w.v, w.do)]
+    q, k, v, do = (t.to(dev) for t in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.fa_bwd_workspace_size(B, H, N, d), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def check(rc):
+        if rc != binding.FA_OK:
+            raise binding.FAError(rc, binding.last_error())
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        check(binding.fa_fwd(q, k, v, o, lse, causal, scale, W["stable"], W["beta"], None, stream))
+        if ev is not None:
+            ev[1].record(stream)
+        check(binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, None, causal, scale, ws, stream,
+                             binding.FA_BWD_PREPROCESS))
+        if ev is not None:
+            ev[2].record(stream)
+        check(binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, None, causal, scale, ws, stream, binding.FA_BWD_MAIN))
+        if ev is not None:
+            ev[3].record(stream)
+        check(binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, None, causal, scale, ws, stream,
+                             binding.FA_BWD_DQ_CONVERT))
+        if ev is not None:
+            ev[4].record(stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    binding.device_status(stream)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    binding.device_status(stream)
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+    bwd_ms = pre_ms + main_ms + conv_ms
+    ms_step = total_ms / K
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    ff, fb = flops_fwd(B, H, N, d, causal), flops_bwd(B, H, N, d, causal)
+    value = (ff + fb) * world / (ms_step * 1e-3) / 1e12
+
+    # ---------------- end to end through the public API, host buffers in and out
+    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+    E = max(3, min(K, 10))
+    for _ in range(2):
+        for hsrc, ddst in zip(host, (q, k, v, do)):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(E):
+        for hsrc, ddst in zip(host, (q, k, v, do)):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        for dsrc, hdst in zip((o, lse, dq, dk, dv), out_host):
+            hdst.copy_(dsrc, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / E
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    binding.device_status(stream)
+
+    peaks = load_peaks()
+    peak = peaks["bf16_tflops"]
+    main_tf = fb / (main_ms * 1e-3) / 1e12
+    fwd_tf = ff / (fwd_ms * 1e-3) / 1e12
+    if main_ms >= fwd_ms:
+        dom = {"kernel": "fa_bwd_main<128>", "achieved": main_tf, "tag": "bwd_main"}
+    else:
+        dom = {"kernel": "fa_fwd_kernel<128,stable>", "achieved": fwd_tf, "tag": "fwd"}
+    roofline = {"bound": "tensor", "kernel": dom["kernel"], "achieved": round(dom["achieved"], 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(dom["achieved"] / peak, 4),
+                "traffic": profiled_traffic(dom["tag"]),
+                "peak_source": f"{peaks['source']} dense BF16 (burst) from MEASURED_PEAKS.json"
+                if peaks["source"] == "measured" else "fallback 1900 TFLOP/s"}
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "LLaMA-7B shaped causal attention B=1 H=32 N=8192 d=128, stabilised shift "
+                               "beta=1.25, fwd+bwd", "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                   "stable": W["stable"], "beta": W["beta"],
+                   "l2": "no flush: q,k,v,dO,o,dq,dk,dv (67 MB each) plus the 134 MB dQ accumulator exceed "
+                         "the 129 MB L2"},
+        "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(fb / (bwd_ms * 1e-3) / 1e12, 1),
+        "bwd_main_tflops": round(main_tf, 1),
+        "fwd_frac_of_peak": round(fwd_tf / peak, 4), "bwd_frac_of_peak": round(fb / (bwd_ms * 1e-3) / 1e12 / peak, 4),
+        "kernel_ms": {"fwd": round(fwd_ms, 4), "bwd_preprocess": round(pre_ms, 4), "bwd_main": round(main_ms, 4),
+                      "bwd_dq_convert": round(conv_ms, 4)},
+        "e2e": {"value": round((ff + fb) * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 4 * K,
+        "roofline": roofline,
+        "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    heads = 1
+    for _ in range(args.warmup):
+        oracle_sample_run(heads)
+    times, fl = [], 0.0
+    for _ in range(args.steps):
+        fl, dt = oracle_sample_run(heads)
+        times.append(dt)
+    ms = statistics.mean(times) * 1e3
+    value = fl / (ms * 1e-3) / 1e12
+    sample = (f"{heads} of 32 heads (N=8192, d=128, causal) forward + backward per step, numpy FP64 oracle on "
+              f"the host cores")
+    W = WORKLOAD
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "LLaMA-7B shaped causal attention B=1 H=32 N=8192 d=128, stabilised shift "
+                               "beta=1.25, fwd+bwd", "B": W["B"], "H": W["H"], "N": W["N"], "d": W["d"],
+                   "causal": W["causal"], "stable": W["stable"], "beta": W["beta"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

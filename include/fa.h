@@ -116,6 +116,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            float scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd_staged -- the same computation as fa_bwd, split into its three
+ * device stages so a caller can schedule or time them separately.  Same
+ * arguments as fa_bwd plus `stages`, a bit mask:
+ *   FA_BWD_PREPROCESS  delta = rowsum(dO o O) and zeroing of the FP32 dQ accumulator
+ *   FA_BWD_MAIN        the recomputing kernel: dK, dV and the dQ accumulator
+ *   FA_BWD_DQ_CONVERT  dq = bf16(scale * dQ accumulator)
+ * The stages must run in this order on the same workspace (the accumulator
+ * lives there between calls); fa_bwd(...) == fa_bwd_staged(..., FA_BWD_ALL).
+ */
+enum { FA_BWD_PREPROCESS = 1, FA_BWD_MAIN = 2, FA_BWD_DQ_CONVERT = 4, FA_BWD_ALL = 7 };
+
+int fa_bwd_staged(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                  void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N, int d, int causal,
+                  float scale, void* workspace, size_t workspace_bytes, void* stream, int stages);
+
+/*
  * fa_device_status -- synchronise `stream`, then return and clear the current
  * device's status word: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_BOUNDS
  * (FA_ERR_CUDA if the synchronisation itself fails).

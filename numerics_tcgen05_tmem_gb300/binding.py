@@ -23,7 +23,10 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_DEVICE_BOUNDS = 5
 
 # every symbol include/fa.h declares
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_device_status", "fa_last_error", "fa_version")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_staged", "fa_bwd_workspace_size", "fa_device_status", "fa_last_error",
+           "fa_version")
+
+FA_BWD_PREPROCESS, FA_BWD_MAIN, FA_BWD_DQ_CONVERT, FA_BWD_ALL = 1, 2, 4, 7
 
 
 class FAError(RuntimeError):
@@ -55,6 +58,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fa_bwd_workspace_size.restype = cs
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, cs, vp]
     L.fa_bwd.restype = ci
+    L.fa_bwd_staged.argtypes = L.fa_bwd.argtypes + [ci]
+    L.fa_bwd_staged.restype = ci
     L.fa_device_status.argtypes = [vp]
     L.fa_device_status.restype = ci
     L.fa_last_error.argtypes = []
@@ -109,12 +114,15 @@ def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(load().fa_bwd_workspace_size(B, H, N, d))
 
 
-def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, delta, causal: bool, scale: float, workspace, stream=None) -> int:
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, delta, causal: bool, scale: float, workspace, stream=None,
+           stages: int = FA_BWD_ALL) -> int:
     B, H, N, d = q.shape
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                         _ptr(delta), B, H, N, d, int(bool(causal)), float(scale), _ptr(workspace), nbytes,
-                         _stream(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(delta),
+            B, H, N, d, int(bool(causal)), float(scale), _ptr(workspace), nbytes, _stream(stream))
+    if stages == FA_BWD_ALL:
+        return load().fa_bwd(*args)
+    return load().fa_bwd_staged(*args, int(stages))
 
 
 def fa_device_status(stream=None) -> int:

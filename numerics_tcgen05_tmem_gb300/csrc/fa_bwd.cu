@@ -441,12 +441,12 @@ namespace {
 template <int D>
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
                void* dk, void* dv, float* delta_out, int B, int H, int N, int causal, float scale, float* dq_acc,
-               float* delta, cudaStream_t stream) {
+               float* delta, cudaStream_t stream, int stages) {
   using namespace fa;
   using C = bwd::Cfg<D>;
   const long long rows = (long long)B * H * N;
   int rc;
-  {
+  if (stages & FA_BWD_PREPROCESS) {
     constexpr int rows_per_block = 8 * (32 / (D / 8));
     const long long grid = (rows + rows_per_block - 1) / rows_per_block;
     bwd::fa_bwd_preprocess<D><<<(unsigned)grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
@@ -454,6 +454,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
                                                                 delta_out, dq_acc, rows);
     if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_preprocess"))) return rc;
   }
+  if (stages & FA_BWD_MAIN) {
   CUtensorMap tq, tk, tv, tdo;
   if ((rc = make_tmap_bhnd(&tq, q, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tk, k, B * H, N, D, bwd::kBlock)) ||
       (rc = make_tmap_bhnd(&tv, v, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tdo, dO, B * H, N, D, bwd::kBlock)))
@@ -478,6 +479,8 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
     return rc;
   kern<<<(unsigned)(p.n_tiles * p.BH), bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
   if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_main"))) return rc;
+  }
+  if (!(stages & FA_BWD_DQ_CONVERT)) return FA_OK;
   const long long n8 = rows * D / 8;
   bwd::fa_bwd_dq_convert<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
                                                                            scale, n8);
@@ -492,12 +495,15 @@ extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return fa::round_up(bhn * d * 4, 256) + fa::round_up(bhn * 4, 256);
 }
 
-extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
-                      void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N, int d, int causal,
-                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" int fa_bwd_staged(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                             const void* dO, void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N,
+                             int d, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
+                             int stages) {
   using namespace fa;
   clear_error();
   int rc;
+  if (stages <= 0 || (stages & ~FA_BWD_ALL))
+    return set_error(FA_ERR_INVALID_ARG, "stages must be a non-empty mask of FA_BWD_* bits (got %d)", stages);
   if ((rc = check_shape(B, H, N, d))) return rc;
   if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) || (rc = check_ptr(o, "o")) ||
       (rc = check_ptr(lse, "lse")) || (rc = check_ptr(dO, "dO")) || (rc = check_ptr(dq, "dq")) ||
@@ -516,7 +522,14 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(bhn * d * 4, 256));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return d == 64 ? launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, dq_acc,
-                                  delta, s)
+                                  delta, s, stages)
                  : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale,
-                                   dq_acc, delta, s);
+                                   dq_acc, delta, s, stages);
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                      void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N, int d, int causal,
+                      float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa_bwd_staged(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, d, causal, scale, workspace,
+                       workspace_bytes, stream, FA_BWD_ALL);
 }
