@@ -132,6 +132,38 @@ int fa_bwd_staged(const void* q, const void* k, const void* v, const void* o, co
                   float scale, void* workspace, size_t workspace_bytes, void* stream, int stages);
 
 /*
+ * fa_bwd_noalloc -- the backward of fa_bwd for callers that cannot allocate device
+ * memory.  (The pages have no counterpart; this is a deployment variant.)
+ *
+ * Some callers cannot call cudaMalloc: a plugin or custom operator inside a host
+ * application that owns the device-memory budget and forbids allocations outside
+ * its pool, or a latency-critical path where cudaMalloc/cudaFree would
+ * synchronise the device.  This entry point allocates nothing: the backward's
+ * scratch (the FP32 dQ accumulator and delta) lives in a fixed file-scope device
+ * array of FA_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading the library
+ * holds until the process exits.  The caller still passes all inputs and outputs.
+ *   - Arguments, layouts and results are those of fa_bwd without the workspace.
+ *   - Problems whose scratch, fa_bwd_workspace_size(B,H,N,d), exceeds 32 MiB are
+ *     rejected with FA_ERR_INVALID_ARG and a message (e.g. B*H*N*d up to about
+ *     8M elements at d = 128).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array and the library zeroes what must
+ *     start at zero on each call; calls that overlap on the GPU (different streams,
+ *     or host threads racing) race on the scratch and give wrong results: serialise
+ *     them.
+ *   - Device-side timeouts of this entry point are recorded in its own static
+ *     status word, not the one fa_device_status() reads.
+ * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N, int d, int causal,
+                   float scale, void* stream);
+
+/*
  * fa_device_status -- synchronise `stream`, then return and clear the current
  * device's status word: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_BOUNDS
  * (FA_ERR_CUDA if the synchronisation itself fails).

@@ -23,8 +23,11 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_DEVICE_BOUNDS = 5
 
 # every symbol include/fa.h declares
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_staged", "fa_bwd_workspace_size", "fa_device_status", "fa_last_error",
-           "fa_version")
+EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_staged", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_device_status",
+           "fa_last_error", "fa_version")
+
+# size of the fixed device scratch behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in fa.h)
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 FA_BWD_PREPROCESS, FA_BWD_MAIN, FA_BWD_DQ_CONVERT, FA_BWD_ALL = 1, 2, 4, 7
 
@@ -60,6 +63,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fa_bwd.restype = ci
     L.fa_bwd_staged.argtypes = L.fa_bwd.argtypes + [ci]
     L.fa_bwd_staged.restype = ci
+    L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp]
+    L.fa_bwd_noalloc.restype = ci
     L.fa_device_status.argtypes = [vp]
     L.fa_device_status.restype = ci
     L.fa_last_error.argtypes = []
@@ -123,6 +128,14 @@ def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, delta, causal: bool, scale: float, w
     if stages == FA_BWD_ALL:
         return load().fa_bwd(*args)
     return load().fa_bwd_staged(*args, int(stages))
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, delta, causal: bool, scale: float, stream=None) -> int:
+    """fa_bwd without a workspace: the library's fixed device scratch is used (nothing is allocated)."""
+    B, H, N, d = q.shape
+    return load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _ptr(delta), B, H, N, d, int(bool(causal)), float(scale),
+                                 _stream(stream))
 
 
 def fa_device_status(stream=None) -> int:

@@ -25,6 +25,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "fa_host.h"
 #include "sm103.cuh"
 
@@ -441,7 +443,7 @@ namespace {
 template <int D>
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
                void* dk, void* dv, float* delta_out, int B, int H, int N, int causal, float scale, float* dq_acc,
-               float* delta, cudaStream_t stream, int stages) {
+               float* delta, cudaStream_t stream, int stages, uint32_t* status_word = nullptr) {
   using namespace fa;
   using C = bwd::Cfg<D>;
   const long long rows = (long long)B * H * N;
@@ -465,7 +467,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   p.dq_acc = dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  p.status = device_status_word();
+  p.status = status_word ? status_word : device_status_word();
   if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
   p.N = N;
   p.BH = B * H;
@@ -532,4 +534,85 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
   return fa_bwd_staged(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, d, causal, scale, workspace,
                        workspace_bytes, stream, FA_BWD_ALL);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Backward without any device allocation.
+//
+// Some callers cannot call cudaMalloc: a plugin or custom operator running inside a host
+// application that owns the device-memory budget and forbids allocations outside its own
+// pool, or a latency-critical path where cudaMalloc/cudaFree would synchronise the device.
+// fa_bwd_noalloc serves them: the backward's scratch (FP32 dQ accumulator and delta) lives in
+// a fixed file-scope device array, so the call itself allocates nothing.  The array's size is
+// fixed at FA_NOALLOC_SCRATCH_BYTES; every GPU that loads this library holds it until exit.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoAllocMaxDevices = 64;
+
+// Scratch shared by every fa_bwd_noalloc call on a device, plus that entry point's own
+// device status word (the library's allocated status word is not used here).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) uint32_t g_noalloc_status;
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+uint32_t* g_noalloc_status_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the static scratch for the current device.  In host code the array's
+// name is only a host-side stand-in, so the address must come from cudaGetSymbolAddress,
+// once per device, with that device current.
+int noalloc_scratch(void** scratch, uint32_t** status) {
+  int dev = 0;
+  int rc = fa::check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fa::set_error(FA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kNoAllocMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    void* s = nullptr;
+    if ((rc = fa::check_cuda(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)"))) return rc;
+    if ((rc = fa::check_cuda(cudaGetSymbolAddress(&s, g_noalloc_status), "cudaGetSymbolAddress(status)"))) return rc;
+    g_noalloc_ptr[dev] = p;
+    g_noalloc_status_ptr[dev] = static_cast<uint32_t*>(s);
+  }
+  *scratch = g_noalloc_ptr[dev];
+  *status = g_noalloc_status_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dO, void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N,
+                              int d, int causal, float scale, void* stream) {
+  using namespace fa;
+  clear_error();
+  int rc;
+  if ((rc = check_shape(B, H, N, d))) return rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) || (rc = check_ptr(o, "o")) ||
+      (rc = check_ptr(lse, "lse")) || (rc = check_ptr(dO, "dO")) || (rc = check_ptr(dq, "dq")) ||
+      (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
+    return rc;
+  if (delta_out && (reinterpret_cast<uintptr_t>(delta_out) & 3))
+    return set_error(FA_ERR_INVALID_ARG, "delta_out is not 4-byte aligned");
+  if (!(scale > 0.f) || !isfinite(scale)) return set_error(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  const size_t need = fa_bwd_workspace_size(B, H, N, d);
+  if (need > kNoAllocScratchBytes)
+    return set_error(FA_ERR_INVALID_ARG,
+                     "problem needs %zu bytes of backward scratch; fa_bwd_noalloc holds at most %zu "
+                     "(use fa_bwd with a caller-allocated workspace)",
+                     need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  uint32_t* status = nullptr;
+  if ((rc = noalloc_scratch(&scratch, &status))) return rc;
+  const size_t bhn = (size_t)B * H * N;
+  float* dq_acc = static_cast<float*>(scratch);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(scratch) + round_up(bhn * d * 4, 256));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, dq_acc,
+                                  delta, s, FA_BWD_ALL, status)
+                 : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale,
+                                   dq_acc, delta, s, FA_BWD_ALL, status);
 }
