@@ -9,18 +9,21 @@
 //   dS = P o (dP - delta),   dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Three kernels on the caller's stream:
-//   fa_bwd_preprocess: delta_i = sum_c dO_ic O_ic (FP32) and dQ_acc = 0
+//   fa_bwd_preprocess: delta_i = sum_c dO_ic O_ic (FP32), lse_i log2(e), both padded per
+//                      head to a multiple of 128 rows, and dQ_acc = 0
 //   fa_bwd_main:       one CTA per (b, h, 128-key tile); loops over query tiles
 //   fa_bwd_dq_convert: dq = bf16(scale * dQ_acc)
 //
-// fa_bwd_main CTA organisation:
-//   warps 0-3  "softmax" warpgroup: thread = key row (TMEM lane) of the tile;
+// fa_bwd_main CTA organisation (448 threads):
+//   warps 0-7  two "softmax" warpgroups; thread = key row (TMEM lane) of the tile,
+//              warpgroup h takes query columns [64h, 64h+64):
 //              P^T = exp2(S^T c - lse_q log2 e) into TMEM (BF16) for the dV MMA,
 //              dS^T = P^T o (dP^T - delta_q) into shared memory (BF16, 128B swizzle)
-//              for the dK and dQ MMAs; finally writes dK and dV.
-//   warps 4-7  dQ warpgroup: thread = query row; reads each dQ tile from TMEM and
-//              adds it into the FP32 dQ accumulator in global memory.
-//   warp  8    MMA issuer;  warp 9  TMA producer.
+//              for the dK and dQ MMAs; finally warpgroup 0 writes dK, 1 writes dV.
+//   warps 8-11 dQ warpgroup: thread = query row; loads each dQ tile from TMEM, hands
+//              the columns back, then reduces it into the FP32 dQ accumulator.
+//   warp  12   MMA issuer;  warp 13  TMA producer (Q, dO tiles and the per-tile
+//              lse / delta vectors, double-buffered).
 // Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -34,9 +37,9 @@ namespace fa {
 namespace bwd {
 
 constexpr int kBlock = 128;     // keys per CTA tile and queries per step
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kThreads = 448;   // 14 warps
+constexpr int kMmaWarp = 12;
+constexpr int kLoadWarp = 13;
 constexpr int kStages = 2;      // query-tile ring depth (Q and dO)
 
 template <int D>
@@ -47,8 +50,10 @@ struct Cfg {
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
   static constexpr int kDSOff = kDOOff + kStages * kTileBytes;     // dS^T, 128 x 128 BF16
-  static constexpr int kBarOff = kDSOff + kBlock * kBlock * 2;
-  static constexpr int kSmemBytes = kBarOff + 512;
+  static constexpr int kLseOff = kDSOff + kBlock * kBlock * 2;      // lse*log2(e), per stage
+  static constexpr int kDeltaOff = kLseOff + kStages * kBlock * 4;   // delta, per stage
+  static constexpr int kBarOff = kDeltaOff + kStages * kBlock * 4;
+  static constexpr int kSmemBytes = kBarOff + 256;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 128, kTmemDK = 256, kTmemDV = 256 + D;
   static constexpr uint32_t kIdescSq = idesc_bf16(128, kBlock, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescKV = idesc_bf16(128, D, false, true);        // dV (TMEM A), dK
@@ -64,35 +69,44 @@ struct Bars {
 };
 
 struct Params {
-  const float* lse;
-  const float* delta;
+  const float* lse2;    // [BH, N_pad] lse * log2(e), +inf past N
+  const float* delta;   // [BH, N_pad] delta, 0 past N
   float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   uint32_t* status;
   int N;
   int BH;
-  int n_tiles;      // ceil(N / 128)
+  int N_pad;        // N rounded up to 128
+  int n_tiles;      // N_pad / 128
   int causal;
   float scale;
   float scale_log2;
 };
 
 // --------------------------------------------------------------------------- preprocess
-// delta = rowsum(dO o O) in FP32 and dQ_acc = 0.  d/8 lanes per row, 16-byte loads.
+// Over the padded rows (bh, q < N_pad): delta = rowsum(dO o O) in FP32, lse2 = lse log2(e)
+// and dQ_acc = 0 for q < N; delta = 0 and lse2 = +inf (so P = 0) for the padding.
+// d/8 lanes per row, 16-byte loads.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dO,
-                                                         float* __restrict__ delta, float* __restrict__ delta_out,
-                                                         float* __restrict__ dq_acc, long long rows) {
+                                                         const float* __restrict__ lse, float* __restrict__ delta,
+                                                         float* __restrict__ lse2, float* __restrict__ delta_out,
+                                                         float* __restrict__ dq_acc, long long rows_pad, int N,
+                                                         int N_pad) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const int lane = threadIdx.x % 32;
   const long long warp_global = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
-  const long long row = warp_global * kRowsPerWarp + lane / kLanesPerRow;
+  const long long prow = warp_global * kRowsPerWarp + lane / kLanesPerRow;
+  const long long bh = prow / N_pad;
+  const int q = (int)(prow - bh * N_pad);
+  const bool valid = prow < rows_pad && q < N;
+  const long long row = bh * N + q;
   const int c = (lane % kLanesPerRow) * 8;
   float acc = 0.f;
-  if (row < rows) {
+  if (valid) {
     const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + c);
     const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + c);
     const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -110,9 +124,10 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __
   }
 #pragma unroll
   for (int off = kLanesPerRow / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && (lane % kLanesPerRow) == 0) {
-    delta[row] = acc;
-    if (delta_out) delta_out[row] = acc;
+  if (prow < rows_pad && (lane % kLanesPerRow) == 0) {
+    delta[prow] = acc;
+    lse2[prow] = valid ? lse[row] * 1.4426950408889634f : INFINITY;
+    if (valid && delta_out) delta_out[row] = acc;
   }
 }
 
@@ -163,9 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.do_empty[s], 1);
     }
     mbar_init(&sh.s_full, 1);
-    mbar_init(&sh.p_ready, kBlock);
+    mbar_init(&sh.p_ready, 2 * kBlock);
     mbar_init(&sh.dp_full, 1);
-    mbar_init(&sh.ds_ready, kBlock);
+    mbar_init(&sh.ds_ready, 2 * kBlock);
     mbar_init(&sh.ds_empty, 1);
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_empty, kBlock);
@@ -193,15 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + C::kKOff + c * 16384, &tmK, &sh.kv_full, c * 64, jt * kBlock, bh);
         tma_load_3d(smem + C::kVOff + c * 16384, &tmV, &sh.kv_full, c * 64, jt * kBlock, bh);
       }
+      const size_t stat_base = (size_t)bh * p.N_pad;
       int nq = 0, ndo = 0;
       for (int it = 0; it < n_it; ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
         const int row0 = (i0 + it) * kBlock;
         if (!mbar_wait(&sh.q_empty[s], ph ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&sh.q_full[s], C::kTileBytes);
+        // Q tile plus the tile's 128 padded lse*log2(e) and delta values (512 B each)
+        mbar_arrive_expect_tx(&sh.q_full[s], C::kTileBytes + 2 * kBlock * 4);
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + C::kQOff + s * C::kTileBytes + c * 16384, &tmQ, &sh.q_full[s], c * 64, row0, bh);
+        bulk_load(smem + C::kLseOff + s * kBlock * 4, p.lse2 + stat_base + row0, kBlock * 4, &sh.q_full[s]);
+        bulk_load(smem + C::kDeltaOff + s * kBlock * 4, p.delta + stat_base + row0, kBlock * 4, &sh.q_full[s]);
         nq = it + 1;
         if (!mbar_wait(&sh.do_empty[s], ph ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&sh.do_full[s], C::kTileBytes);
@@ -254,12 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kTmemDP, kmaj(sV, kk), kmaj(dO, kk), C::kIdescSq, kk > 0);
         tc_commit(&sh.dp_full);
-        // dV += P^T dO_i   (P^T from TMEM, 8 columns per k-step of 16 queries)
+        // dV += P^T dO_i: P^T (BF16) sits in S^T's columns 0-31 (queries 0-63) and
+        // 64-95 (queries 64-127); 8 columns per k-step of 16 queries
         if (!(ok = mbar_wait(&sh.p_ready, it & 1, abort_flag, p.status))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk)
-          mma_ts(tmem + C::kTmemDV, tmem + C::kTmemS + kk * 8, mnmaj(dO, kk), C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kTmemDV, tmem + C::kTmemS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(dO, kk),
+                 C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sh.do_empty[s]);
         // next S^T (overwrites P^T only after the dV MMA above has read it: same-thread MMAs run in order)
         if (it + 1 < n_it) {
@@ -282,55 +303,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(&sh.mma_done);
       mbar_wait(&sh.mma_done, 0, abort_flag, p.status);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ P^T / dS^T warpgroup
-    const int lane_base = warp * 32;
-    const int r = lane_base + (threadIdx.x % 32);  // key row within the tile
-    const int key = jt * kBlock + r;
-    const uint32_t tS = tmem + C::kTmemS + ((uint32_t)lane_base << 16);
-    const uint32_t tDP = tmem + C::kTmemDP + ((uint32_t)lane_base << 16);
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ P^T / dS^T warpgroups
+    // warpgroup h handles query columns [64h, 64h + 64) of every key row
+    const int h = warp / 4;
+    const int lane_base = (warp % 4) * 32;
+    const int r = lane_base + (threadIdx.x % 32);  // key row within the tile (= TMEM lane)
+    const uint32_t lane_off = (uint32_t)lane_base << 16;
+    const uint32_t tS = tmem + C::kTmemS + lane_off + 64 * h;
+    const uint32_t tDP = tmem + C::kTmemDP + lane_off + 64 * h;
     const float c = p.scale_log2;
-    const float* lse = p.lse + (size_t)bh * p.N;
-    const float* dl = p.delta + (size_t)bh * p.N;
-    uint8_t* ds_row = smem + C::kDSOff + r * 128;
+    uint8_t* ds_row = smem + C::kDSOff + h * 16384 + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int q0 = (i0 + it) * kBlock;
-      // visible queries of this key row: q >= key when causal, q < N always
-      const int qlo = p.causal ? key - q0 : 0;   // first visible column
-      const int qhi = p.N - q0;                  // one past the last visible column
+      const int s = it % kStages;
+      const bool diag = p.causal && it == 0;  // query tile i0 == key tile jt: mask q < key
+      const float4* lse4 = reinterpret_cast<const float4*>(smem + C::kLseOff + s * kBlock * 4) + 16 * h;
+      const float4* dl4 = reinterpret_cast<const float4*>(smem + C::kDeltaOff + s * kBlock * 4) + 16 * h;
+      if (!(ok = mbar_wait(&sh.q_full[s], (it / kStages) & 1, abort_flag, p.status))) break;
       if (!(ok = mbar_wait(&sh.s_full, it & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      float pr[kBlock];
+      // P^T = exp2(S^T c - lse_q log2 e); padded queries carry lse = +inf -> 0
+      float pr[64];
 #pragma unroll
-      for (int c0 = 0; c0 < kBlock; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t w[32];
         tmem_ld32(tS + c0, w);
         tmem_ld_wait();
         reg_fence(w);
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          const int qc = c0 + i;
-          float lv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) lv[u] = (q0 + qc + u < p.N) ? __ldg(lse + q0 + qc + u) : 0.f;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const bool vis = (qc + u >= qlo) && (qc + u < qhi) && (key < p.N);
-            const float e = ex2_approx(fmaf(__uint_as_float(w[i + u]), c, -lv[u] * 1.4426950408889634f));
-            pr[qc + u] = vis ? e : 0.f;
-          }
+          const float4 l4 = lse4[(c0 + i) / 4];
+          pr[c0 + i + 0] = ex2_approx(fmaf(__uint_as_float(w[i + 0]), c, -l4.x));
+          pr[c0 + i + 1] = ex2_approx(fmaf(__uint_as_float(w[i + 1]), c, -l4.y));
+          pr[c0 + i + 2] = ex2_approx(fmaf(__uint_as_float(w[i + 2]), c, -l4.z));
+          pr[c0 + i + 3] = ex2_approx(fmaf(__uint_as_float(w[i + 3]), c, -l4.w));
         }
+      }
+      if (diag) {
+        // query column 64h + j is visible to key row r iff 64h + j >= r
+#pragma unroll
+        for (int j = 0; j < 64; ++j) pr[j] = (64 * h + j >= r) ? pr[j] : 0.f;
       }
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[h * 64 + 2 * i], pr[h * 64 + 2 * i + 1]);
-          tmem_st32(tS + h * 32, pk);
-        }
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+        __syncwarp();
+        tmem_st32(tS, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -341,89 +362,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it > 0 && !(ok = mbar_wait(&sh.ds_empty, (it - 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c0 = 0; c0 < kBlock; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t w[32];
         tmem_ld32(tDP + c0, w);
         tmem_ld_wait();
         reg_fence(w);
-        uint32_t dsk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const int qc = c0 + i;
-          float d4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) d4[u] = (q0 + qc + u < p.N) ? __ldg(dl + q0 + qc + u) : 0.f;
-          dsk[i / 2] = pack_bf16x2(pr[qc] * (__uint_as_float(w[i]) - d4[0]),
-                                   pr[qc + 1] * (__uint_as_float(w[i + 1]) - d4[1]));
-          dsk[i / 2 + 1] = pack_bf16x2(pr[qc + 2] * (__uint_as_float(w[i + 2]) - d4[2]),
-                                       pr[qc + 3] * (__uint_as_float(w[i + 3]) - d4[3]));
-        }
-        // row r of dS^T, 16-byte chunk g (8 queries) -> block g/8, swizzled chunk (g%8) ^ (r%8)
+        // row r of dS^T, 16-byte chunk g (8 queries) of this 64-query block, swizzled (g ^ r%8)
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
-          const int g = c0 / 8 + gg;
-          *reinterpret_cast<uint4*>(ds_row + (g / 8) * 16384 + ((((uint32_t)g % 8) ^ sw) << 4)) =
-              make_uint4(dsk[4 * gg], dsk[4 * gg + 1], dsk[4 * gg + 2], dsk[4 * gg + 3]);
+          const int i = gg * 8;
+          const float4 da = dl4[(c0 + i) / 4], db = dl4[(c0 + i) / 4 + 1];
+          const float* pp = pr + c0 + i;
+          const uint4 v4 = make_uint4(pack_bf16x2(pp[0] * (__uint_as_float(w[i + 0]) - da.x), pp[1] * (__uint_as_float(w[i + 1]) - da.y)),
+                                      pack_bf16x2(pp[2] * (__uint_as_float(w[i + 2]) - da.z), pp[3] * (__uint_as_float(w[i + 3]) - da.w)),
+                                      pack_bf16x2(pp[4] * (__uint_as_float(w[i + 4]) - db.x), pp[5] * (__uint_as_float(w[i + 5]) - db.y)),
+                                      pack_bf16x2(pp[6] * (__uint_as_float(w[i + 6]) - db.z), pp[7] * (__uint_as_float(w[i + 7]) - db.w)));
+          const uint32_t g = (uint32_t)(c0 / 8 + gg);
+          *reinterpret_cast<uint4*>(ds_row + ((g ^ sw) << 4)) = v4;
         }
       }
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&sh.ds_ready);
     }
-    // ------------------------------------------------------------------ dK, dV epilogue
+    // ------------------------------------------------------------------ dK (h = 0) / dV (h = 1) epilogue
     if (ok && n_it > 0 && mbar_wait(&sh.mma_done, 0, abort_flag, p.status)) {
       tc_fence_after();
+      const int key = jt * kBlock + r;
       const bool valid = key < p.N;
       const size_t orow = ((size_t)bh * p.N + (valid ? key : 0)) * D;
+      const uint32_t t = tmem + (h == 0 ? C::kTmemDK : C::kTmemDV) + lane_off;
+      const float mul = h == 0 ? p.scale : 1.f;
+      __nv_bfloat16* out = h == 0 ? p.dk : p.dv;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t t = tmem + (which == 0 ? C::kTmemDK : C::kTmemDV) + ((uint32_t)lane_base << 16);
-        const float mul = which == 0 ? p.scale : 1.f;
-        __nv_bfloat16* out = which == 0 ? p.dk : p.dv;
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t w[32];
+        tmem_ld32(t + c0, w);
+        tmem_ld_wait();
+        reg_fence(w);
+        uint4 pkd[4];
+        uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t w[32];
-          tmem_ld32(t + c0, w);
-          tmem_ld_wait();
-          reg_fence(w);
-          uint4 pkd[4];
-          uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+        for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + orow + c0);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + orow + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
-          }
+          for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
         }
       }
     }
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     // ------------------------------------------------------------------ dQ warpgroup
-    const int lane_base = (warp - 4) * 32;
+    const int lane_base = (warp % 4) * 32;
     const int r = lane_base + (threadIdx.x % 32);  // query row within the current query tile
     const uint32_t tDQ = tmem + C::kTmemDQ + ((uint32_t)lane_base << 16);
     for (int it = 0; it < n_it; ++it) {
       if (!mbar_wait(&sh.dq_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
+      // load the row in two halves; the columns go back to the MMA warp right after the
+      // second load, before the reductions of that half are issued
       const int qrow = (i0 + it) * kBlock + r;
       float* dst = p.dq_acc + ((size_t)bh * p.N + (qrow < p.N ? qrow : 0)) * D;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t w[32];
-        tmem_ld32(tDQ + c0, w);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[D / 2];
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32)
+          tmem_ld32(tDQ + half * (D / 2) + c0, *reinterpret_cast<uint32_t(*)[32]>(w + c0));
         tmem_ld_wait();
         reg_fence(w);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&sh.dq_empty);
+        }
         if (qrow < p.N) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + c0 + i),
-                      make_float4(__uint_as_float(w[i]), __uint_as_float(w[i + 1]), __uint_as_float(w[i + 2]),
-                                  __uint_as_float(w[i + 3])));
+          for (int i = 0; i < D / 2; i += 4) red_add_v4(dst + half * (D / 2) + i, w[i], w[i + 1], w[i + 2], w[i + 3]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&sh.dq_empty);
     }
   }
 
@@ -440,20 +456,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
+// The backward's scratch, carved from one caller buffer: the FP32 dQ accumulator
+// [BH, N, d], then delta and lse*log2(e) padded per head to N_pad = ceil(N/128)*128 rows,
+// each region 256-byte aligned.
+struct Scratch {
+  float* dq_acc;
+  float* delta;
+  float* lse2;
+};
+
+size_t scratch_bytes(int B, int H, int N, int d) {
+  const size_t bh = (size_t)B * H;
+  const size_t n_pad = ((size_t)N + 127) / 128 * 128;
+  return fa::round_up(bh * N * d * 4, 256) + 2 * fa::round_up(bh * n_pad * 4, 256);
+}
+
+Scratch carve_scratch(void* base, int B, int H, int N, int d) {
+  const size_t bh = (size_t)B * H;
+  const size_t n_pad = ((size_t)N + 127) / 128 * 128;
+  char* p = static_cast<char*>(base);
+  Scratch s;
+  s.dq_acc = reinterpret_cast<float*>(p);
+  p += fa::round_up(bh * N * d * 4, 256);
+  s.delta = reinterpret_cast<float*>(p);
+  p += fa::round_up(bh * n_pad * 4, 256);
+  s.lse2 = reinterpret_cast<float*>(p);
+  return s;
+}
+
 template <int D>
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
-               void* dk, void* dv, float* delta_out, int B, int H, int N, int causal, float scale, float* dq_acc,
-               float* delta, cudaStream_t stream, int stages, uint32_t* status_word = nullptr) {
+               void* dk, void* dv, float* delta_out, int B, int H, int N, int causal, float scale,
+               const Scratch& sc, cudaStream_t stream, int stages, uint32_t* status_word = nullptr) {
   using namespace fa;
   using C = bwd::Cfg<D>;
   const long long rows = (long long)B * H * N;
   int rc;
+  const int N_pad = (N + bwd::kBlock - 1) / bwd::kBlock * bwd::kBlock;
   if (stages & FA_BWD_PREPROCESS) {
     constexpr int rows_per_block = 8 * (32 / (D / 8));
-    const long long grid = (rows + rows_per_block - 1) / rows_per_block;
-    bwd::fa_bwd_preprocess<D><<<(unsigned)grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(o),
-                                                                static_cast<const __nv_bfloat16*>(dO), delta,
-                                                                delta_out, dq_acc, rows);
+    const long long rows_pad = (long long)B * H * N_pad;
+    const long long grid = (rows_pad + rows_per_block - 1) / rows_per_block;
+    bwd::fa_bwd_preprocess<D><<<(unsigned)grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dO), lse, sc.delta, sc.lse2,
+        delta_out, sc.dq_acc, rows_pad, N, N_pad);
     if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_preprocess"))) return rc;
   }
   if (stages & FA_BWD_MAIN) {
@@ -462,16 +508,17 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
       (rc = make_tmap_bhnd(&tv, v, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tdo, dO, B * H, N, D, bwd::kBlock)))
     return rc;
   bwd::Params p{};
-  p.lse = lse;
-  p.delta = delta;
-  p.dq_acc = dq_acc;
+  p.lse2 = sc.lse2;
+  p.delta = sc.delta;
+  p.dq_acc = sc.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status_word ? status_word : device_status_word();
   if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
   p.N = N;
   p.BH = B * H;
-  p.n_tiles = (N + bwd::kBlock - 1) / bwd::kBlock;
+  p.N_pad = N_pad;
+  p.n_tiles = N_pad / bwd::kBlock;
   p.causal = causal;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -484,7 +531,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   }
   if (!(stages & FA_BWD_DQ_CONVERT)) return FA_OK;
   const long long n8 = rows * D / 8;
-  bwd::fa_bwd_dq_convert<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(dq_acc, static_cast<__nv_bfloat16*>(dq),
+  bwd::fa_bwd_dq_convert<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(sc.dq_acc, static_cast<__nv_bfloat16*>(dq),
                                                                            scale, n8);
   return check_cuda(cudaGetLastError(), "launch fa_bwd_dq_convert");
 }
@@ -493,8 +540,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
 
 extern "C" size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (fa::check_shape(B, H, N, d)) return 0;
-  const size_t bhn = (size_t)B * H * N;
-  return fa::round_up(bhn * d * 4, 256) + fa::round_up(bhn * 4, 256);
+  return scratch_bytes(B, H, N, d);
 }
 
 extern "C" int fa_bwd_staged(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -519,14 +565,12 @@ extern "C" int fa_bwd_staged(const void* q, const void* k, const void* v, const 
     return set_error(FA_ERR_INVALID_ARG, "workspace must be a 256-byte aligned device pointer");
   if (workspace_bytes < need)
     return set_error(FA_ERR_INVALID_ARG, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
-  const size_t bhn = (size_t)B * H * N;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(bhn * d * 4, 256));
+  const Scratch sc = carve_scratch(workspace, B, H, N, d);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, dq_acc,
-                                  delta, s, stages)
-                 : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale,
-                                   dq_acc, delta, s, stages);
+  return d == 64 ? launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, sc, s,
+                                  stages)
+                 : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, sc, s,
+                                   stages);
 }
 
 extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
@@ -607,12 +651,10 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
   void* scratch = nullptr;
   uint32_t* status = nullptr;
   if ((rc = noalloc_scratch(&scratch, &status))) return rc;
-  const size_t bhn = (size_t)B * H * N;
-  float* dq_acc = static_cast<float*>(scratch);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(scratch) + round_up(bhn * d * 4, 256));
+  const Scratch sc = carve_scratch(scratch, B, H, N, d);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, dq_acc,
-                                  delta, s, FA_BWD_ALL, status)
-                 : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale,
-                                   dq_acc, delta, s, FA_BWD_ALL, status);
+  return d == 64 ? launch_bwd<64>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, sc, s,
+                                  FA_BWD_ALL, status)
+                 : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, sc, s,
+                                   FA_BWD_ALL, status);
 }
