@@ -265,16 +265,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kBlockN; ++i) sv[i] = (i < lim) ? sv[i] : -INFINITY;
       }
-      float bm = sv[0];
+      // block max with 3-input max over four independent chains
+      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-      for (int i = 1; i < kBlockN; ++i) bm = fmaxf(bm, sv[i]);
+      for (int i = 4; i < kBlockN - 4; i += 8) {
+        mx0 = max3f(mx0, sv[i], sv[i + 1]);
+        mx1 = max3f(mx1, sv[i + 2], sv[i + 3]);
+        mx2 = max3f(mx2, sv[i + 4], sv[i + 5]);
+        mx3 = max3f(mx3, sv[i + 6], sv[i + 7]);
+      }
+      mx0 = max3f(mx0, sv[kBlockN - 4], sv[kBlockN - 3]);
+      mx1 = max3f(mx1, sv[kBlockN - 2], sv[kBlockN - 1]);
+      const float bm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       float m_new;
       if constexpr (kStable || kStats) {
-        // running (max, count) merge: rs' = [rm == rm'] rs + [bm == rm'] bc
+        // running (max, count) merge: rs' = [rm == rm'] rs + [bm == rm'] bc.  The block's
+        // count only matters when bm reaches the running max, so a warp whose rows all
+        // have bm < rm skips counting.
         int bc = 0;
+        if (__any_sync(0xffffffffu, bm >= rm)) {
 #pragma unroll
-        for (int i = 0; i < kBlockN; ++i) bc += (sv[i] == bm) ? 1 : 0;
-        bc = (bm == -INFINITY) ? 0 : bc;
+          for (int i = 0; i < kBlockN; ++i) bc += (sv[i] == bm) ? 1 : 0;
+          bc = (bm == -INFINITY) ? 0 : bc;
+        }
         const float rm_new = fmaxf(rm, bm);
         rs = ((rm == rm_new) ? rs : 0) + ((bm == rm_new) ? bc : 0);
         rm = rm_new;
@@ -295,10 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sum0 = 0.f, sum1 = 0.f;
 #pragma unroll
       for (int i = 0; i < kBlockN; i += 2) {
-        const float p0 = ex2_approx(fmaf(sv[i], c, nmc));
-        const float p1 = ex2_approx(fmaf(sv[i + 1], c, nmc));
-        sum0 += p0;
-        sum1 += p1;
+        float x0, x1;
+        fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);   // scale*log2(e) * (S - m)
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        add2(sum0, sum1, sum0, sum1, p0, p1);
         pk[i / 2] = pack_bf16x2(p0, p1);
       }
       if constexpr (kStats) {
@@ -329,7 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           reg_fence(w);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            float a0, a1;
+            mul2(a0, a1, __uint_as_float(w[i]), __uint_as_float(w[i + 1]), alpha, alpha);
+            w[i] = __float_as_uint(a0);
+            w[i + 1] = __float_as_uint(a1);
+          }
           tmem_st32(tO + c0, w);
         }
         tmem_st_wait();
