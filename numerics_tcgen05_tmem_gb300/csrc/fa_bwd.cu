@@ -335,10 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 l4 = lse4[(c0 + i) / 4];
-          pr[c0 + i + 0] = ex2_approx(fmaf(__uint_as_float(w[i + 0]), c, -l4.x));
-          pr[c0 + i + 1] = ex2_approx(fmaf(__uint_as_float(w[i + 1]), c, -l4.y));
-          pr[c0 + i + 2] = ex2_approx(fmaf(__uint_as_float(w[i + 2]), c, -l4.z));
-          pr[c0 + i + 3] = ex2_approx(fmaf(__uint_as_float(w[i + 3]), c, -l4.w));
+          float x0, x1, x2, x3;
+          fma2(x0, x1, __uint_as_float(w[i + 0]), __uint_as_float(w[i + 1]), c, c, -l4.x, -l4.y);
+          fma2(x2, x3, __uint_as_float(w[i + 2]), __uint_as_float(w[i + 3]), c, c, -l4.z, -l4.w);
+          pr[c0 + i + 0] = ex2_approx(x0);
+          pr[c0 + i + 1] = ex2_approx(x1);
+          pr[c0 + i + 2] = ex2_approx(x2);
+          pr[c0 + i + 3] = ex2_approx(x3);
         }
       }
       if (diag) {
@@ -373,12 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int i = gg * 8;
           const float4 da = dl4[(c0 + i) / 4], db = dl4[(c0 + i) / 4 + 1];
           const float* pp = pr + c0 + i;
-          const uint4 v4 = make_uint4(pack_bf16x2(pp[0] * (__uint_as_float(w[i + 0]) - da.x), pp[1] * (__uint_as_float(w[i + 1]) - da.y)),
-                                      pack_bf16x2(pp[2] * (__uint_as_float(w[i + 2]) - da.z), pp[3] * (__uint_as_float(w[i + 3]) - da.w)),
-                                      pack_bf16x2(pp[4] * (__uint_as_float(w[i + 4]) - db.x), pp[5] * (__uint_as_float(w[i + 5]) - db.y)),
-                                      pack_bf16x2(pp[6] * (__uint_as_float(w[i + 6]) - db.z), pp[7] * (__uint_as_float(w[i + 7]) - db.w)));
-          const uint32_t g = (uint32_t)(c0 / 8 + gg);
-          *reinterpret_cast<uint4*>(ds_row + ((g ^ sw) << 4)) = v4;
+          float g[8];
+          // g = P * (dP - delta), two lanes per instruction
+          add2(g[0], g[1], __uint_as_float(w[i + 0]), __uint_as_float(w[i + 1]), -da.x, -da.y);
+          add2(g[2], g[3], __uint_as_float(w[i + 2]), __uint_as_float(w[i + 3]), -da.z, -da.w);
+          add2(g[4], g[5], __uint_as_float(w[i + 4]), __uint_as_float(w[i + 5]), -db.x, -db.y);
+          add2(g[6], g[7], __uint_as_float(w[i + 6]), __uint_as_float(w[i + 7]), -db.z, -db.w);
+          mul2(g[0], g[1], g[0], g[1], pp[0], pp[1]);
+          mul2(g[2], g[3], g[2], g[3], pp[2], pp[3]);
+          mul2(g[4], g[5], g[4], g[5], pp[4], pp[5]);
+          mul2(g[6], g[7], g[6], g[7], pp[6], pp[7]);
+          const uint4 v4 = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
+                                      pack_bf16x2(g[6], g[7]));
+          const uint32_t chunk = (uint32_t)(c0 / 8 + gg);
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ sw) << 4)) = v4;
         }
       }
       tc_fence_before();
