@@ -40,7 +40,7 @@ constexpr int kBlock = 128;     // keys per CTA tile and queries per step
 constexpr int kThreads = 448;   // 14 warps
 constexpr int kMmaWarp = 12;
 constexpr int kLoadWarp = 13;
-constexpr int kStages = 2;      // query-tile ring depth (Q and dO)
+constexpr int kStages = 2;      // Q-tile ring depth (dO is single-buffered)
 
 template <int D>
 struct Cfg {
@@ -49,8 +49,12 @@ struct Cfg {
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;     // dS^T, 128 x 128 BF16
-  static constexpr int kLseOff = kDSOff + kBlock * kBlock * 2;      // lse*log2(e), per stage
+  static constexpr int kDSOff = kDOOff + kTileBytes;                // dS^T, 128 x 128 BF16
+  // dQ staging: half a dQ tile (128 rows x D/2 FP32 columns) as 128B-swizzled boxes of
+  // 32 columns x 128 rows, the source of the TMA reduce-add into the accumulator
+  static constexpr int kDQBoxes = D / 64;
+  static constexpr int kDQOff = kDSOff + kBlock * kBlock * 2;
+  static constexpr int kLseOff = kDQOff + kDQBoxes * 16384;          // lse*log2(e), per stage
   static constexpr int kDeltaOff = kLseOff + kStages * kBlock * 4;   // delta, per stage
   static constexpr int kBarOff = kDeltaOff + kStages * kBlock * 4;
   static constexpr int kSmemBytes = kBarOff + 256;
@@ -62,7 +66,7 @@ struct Cfg {
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t q_full[kStages], q_empty[kStages], do_full[kStages], do_empty[kStages];
+  uint64_t q_full[kStages], q_empty[kStages], do_full, do_empty;
   uint64_t s_full, p_ready, dp_full, ds_ready, ds_empty, dq_full, dq_empty, mma_done;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -151,7 +155,8 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const Params p) {
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                const __grid_constant__ CUtensorMap tmDQ, const Params p) {
   using C = Cfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // The swizzled operand layouts need a 1024-byte aligned base; there is no slack
@@ -174,9 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh.q_full[s], 1);
       mbar_init(&sh.q_empty[s], 1);
-      mbar_init(&sh.do_full[s], 1);
-      mbar_init(&sh.do_empty[s], 1);
     }
+    mbar_init(&sh.do_full, 1);
+    mbar_init(&sh.do_empty, 1);
     mbar_init(&sh.s_full, 1);
     mbar_init(&sh.p_ready, 2 * kBlock);
     mbar_init(&sh.dp_full, 1);
@@ -222,10 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(smem + C::kLseOff + s * kBlock * 4, p.lse2 + stat_base + row0, kBlock * 4, &sh.q_full[s]);
         bulk_load(smem + C::kDeltaOff + s * kBlock * 4, p.delta + stat_base + row0, kBlock * 4, &sh.q_full[s]);
         nq = it + 1;
-        if (!mbar_wait(&sh.do_empty[s], ph ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&sh.do_full[s], C::kTileBytes);
+        if (!mbar_wait(&sh.do_empty, (it & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::kDOOff + s * C::kTileBytes + c * 16384, &tmDO, &sh.do_full[s], c * 64, row0, bh);
+          tma_load_3d(smem + C::kDOOff + c * 16384, &tmDO, &sh.do_full, c * 64, row0, bh);
         ndo = it + 1;
       }
       if (*abort_flag) {
@@ -234,8 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&sh.kv_full, 0, &ignore_abort, p.status);
         for (int it = max(0, nq - kStages); it < nq; ++it)
           mbar_wait(&sh.q_full[it % kStages], (it / kStages) & 1, &ignore_abort, p.status);
-        for (int it = max(0, ndo - kStages); it < ndo; ++it)
-          mbar_wait(&sh.do_full[it % kStages], (it / kStages) & 1, &ignore_abort, p.status);
+        if (ndo > 0) mbar_wait(&sh.do_full, (ndo - 1) & 1, &ignore_abort, p.status);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -258,35 +262,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kTmemS, kmaj(sK, kk), kmaj(q, kk), C::kIdescSq, kk > 0);
         tc_commit(&sh.s_full);
       };
-      if (ok && n_it > 0) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        const uint32_t q = sQ + s * C::kTileBytes, dO = sDO + s * C::kTileBytes;
-        // dP^T = V_j dO_i^T   (its columns hold the previous dQ tile: wait until drained)
-        if (!(ok = mbar_wait(&sh.do_full[s], ph, abort_flag, p.status))) break;
-        if (it > 0 && !(ok = mbar_wait(&sh.dq_empty, (it - 1) & 1, abort_flag, p.status))) break;
+      const uint32_t dO = sDO;
+      // dP^T = V_j dO_i^T into dP^T's columns (which held dQ_{i-1}: wait until drained)
+      auto issue_dp = [&](int it) {
+        if (!(ok = mbar_wait(&sh.do_full, it & 1, abort_flag, p.status))) return;
+        if (it > 0 && !(ok = mbar_wait(&sh.dq_empty, (it - 1) & 1, abort_flag, p.status))) return;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kTmemDP, kmaj(sV, kk), kmaj(dO, kk), C::kIdescSq, kk > 0);
         tc_commit(&sh.dp_full);
-        // dV += P^T dO_i: P^T (BF16) sits in S^T's columns 0-31 (queries 0-63) and
-        // 64-95 (queries 64-127); 8 columns per k-step of 16 queries
-        if (!(ok = mbar_wait(&sh.p_ready, it & 1, abort_flag, p.status))) break;
+      };
+      // dV += P^T dO_i: P^T (BF16) sits in S^T's columns 0-31 (queries 0-63) and
+      // 64-95 (queries 64-127); 8 columns per k-step of 16 queries
+      auto issue_dv = [&](int it) {
+        if (!(ok = mbar_wait(&sh.do_full, it & 1, abort_flag, p.status))) return;
+        if (!(ok = mbar_wait(&sh.p_ready, it & 1, abort_flag, p.status))) return;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk)
           mma_ts(tmem + C::kTmemDV, tmem + C::kTmemS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(dO, kk),
                  C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&sh.do_empty[s]);
-        // next S^T (overwrites P^T only after the dV MMA above has read it: same-thread MMAs run in order)
-        if (it + 1 < n_it) {
-          issue_s(it + 1);
-          if (!ok) break;
-        }
+      };
+      // Issue order (same-thread MMAs execute in order):
+      //   S_0 dP_0 dV_0 S_1 | dK_0 dQ_0 dV_1 dP_1 S_2 | dK_1 dQ_1 dV_2 dP_2 S_3 | ...
+      // so dK_i/dQ_i run while the softmax warpgroups compute P_{i+1}, and dV_{i+1} runs
+      // while dQ_i is drained from the columns dP_{i+1} needs.
+      if (ok && n_it > 0) {
+        tc_fence_after();
+        issue_s(0);
+        if (ok) issue_dp(0);
+        if (ok) issue_dv(0);
+        if (ok) tc_commit(&sh.do_empty);
+        if (ok && n_it > 1) issue_s(1);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it % kStages;
+        const uint32_t q = sQ + s * C::kTileBytes;
         // dK += dS^T Q_i ;  dQ_i = dS K_j
         if (!(ok = mbar_wait(&sh.ds_ready, it & 1, abort_flag, p.status))) break;
         tc_fence_after();
@@ -299,6 +310,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&sh.q_empty[s]);
         tc_commit(&sh.ds_empty);
         tc_commit(&sh.dq_full);
+        if (it + 1 < n_it) {
+          issue_dv(it + 1);
+          if (!ok) break;
+          issue_dp(it + 1);
+          if (!ok) break;
+          tc_commit(&sh.do_empty);
+          if (it + 2 < n_it) {
+            issue_s(it + 2);
+            if (!ok) break;
+          }
+        }
       }
       tc_commit(&sh.mma_done);
       mbar_wait(&sh.mma_done, 0, abort_flag, p.status);
@@ -424,16 +446,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 12) {
     // ------------------------------------------------------------------ dQ warpgroup
+    // Each dQ tile leaves TMEM in two halves of D/2 columns; a half is written, one row per
+    // thread, into the 128B-swizzled staging boxes and pushed into the FP32 accumulator by
+    // TMA reduce-adds issued by one thread (rows past N are dropped by the hardware).
     const int lane_base = (warp % 4) * 32;
     const int r = lane_base + (threadIdx.x % 32);  // query row within the current query tile
+    const bool leader = (r == 0);
     const uint32_t tDQ = tmem + C::kTmemDQ + ((uint32_t)lane_base << 16);
+    uint8_t* stage_row = smem + C::kDQOff + r * 128;
+    const uint32_t sw = (uint32_t)(r & 7);
     for (int it = 0; it < n_it; ++it) {
       if (!mbar_wait(&sh.dq_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
-      // load the row in two halves; the columns go back to the MMA warp right after the
-      // second load, before the reductions of that half are issued
-      const int qrow = (i0 + it) * kBlock + r;
-      float* dst = p.dq_acc + ((size_t)bh * p.N + (qrow < p.N ? qrow : 0)) * D;
+      const int q0 = (i0 + it) * kBlock;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t w[D / 2];
@@ -443,15 +468,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         reg_fence(w);
         if (half == 1) {
+          // the whole tile is in registers: hand the columns back to the MMA warp
           tc_fence_before();
           mbar_arrive(&sh.dq_empty);
         }
-        if (qrow < p.N) {
+        // the staging boxes are free once the previous reductions have read them
+        if (leader) bulk_wait_read_all();
+        named_barrier(1, kBlock);
 #pragma unroll
-          for (int i = 0; i < D / 2; i += 4) red_add_v4(dst + half * (D / 2) + i, w[i], w[i + 1], w[i + 2], w[i + 3]);
+        for (int b = 0; b < C::kDQBoxes; ++b)
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(stage_row + b * 16384 + (((uint32_t)ch ^ sw) << 4)) =
+                make_uint4(w[b * 32 + ch * 4], w[b * 32 + ch * 4 + 1], w[b * 32 + ch * 4 + 2], w[b * 32 + ch * 4 + 3]);
+        fence_proxy_async_smem();
+        named_barrier(1, kBlock);
+        if (leader) {
+#pragma unroll
+          for (int b = 0; b < C::kDQBoxes; ++b)
+            tma_reduce_add_3d(&tmDQ, smem + C::kDQOff + b * 16384, half * (D / 2) + b * 32, q0, bh);
+          bulk_commit_group();
         }
       }
     }
+    // the accumulator must hold every reduction before the CTA retires
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -515,8 +556,10 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   }
   if (stages & FA_BWD_MAIN) {
   CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tdq;
   if ((rc = make_tmap_bhnd(&tq, q, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tk, k, B * H, N, D, bwd::kBlock)) ||
-      (rc = make_tmap_bhnd(&tv, v, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tdo, dO, B * H, N, D, bwd::kBlock)))
+      (rc = make_tmap_bhnd(&tv, v, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tdo, dO, B * H, N, D, bwd::kBlock)) ||
+      (rc = make_tmap_f32_bhnd(&tdq, sc.dq_acc, B * H, N, D, bwd::kBlock)))
     return rc;
   bwd::Params p{};
   p.lse2 = sc.lse2;
@@ -537,7 +580,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if ((rc = check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                        "cudaFuncSetAttribute(bwd)")))
     return rc;
-  kern<<<(unsigned)(p.n_tiles * p.BH), bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<(unsigned)(p.n_tiles * p.BH), bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_main"))) return rc;
   }
   if (!(stages & FA_BWD_DQ_CONVERT)) return FA_OK;

@@ -65,7 +65,8 @@ int sm_count() {
   return g_sms[dev];
 }
 
-int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+static int encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, int BH, int N,
+                     int d, int box_cols, int box_rows) {
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_encode) {
@@ -78,14 +79,21 @@ int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int
     }
   }
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)d * elem_bytes, (cuuint64_t)N * d * elem_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return FA_OK;
+}
+
+int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, BH, N, d, 64, box_rows);
+}
+
+int make_tmap_f32_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, BH, N, d, 32, box_rows);
 }
 
 int check_shape(int B, int H, int N, int d) {
