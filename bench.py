@@ -47,6 +47,21 @@ def flops_bwd(B, H, N, d, causal):
     return 2.5 * flops_fwd(B, H, N, d, causal)
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The largest value of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job TFLOP/s: every rank's work divided by the slowest rank's time (weak scaling)."""
+    return flops_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -251,13 +266,9 @@ def run_native(args):
     main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
     conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
     bwd_ms = pre_ms + main_ms + conv_ms
-    ms_step = total_ms / K
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / K, dist, dev)
     ff, fb = flops_fwd(B, H, N, d, causal), flops_bwd(B, H, N, d, causal)
-    value = (ff + fb) * world / (ms_step * 1e-3) / 1e12
+    value = job_throughput(ff + fb, world, ms_step)
 
     # ---------------- end to end through the public API, host buffers in and out
     # Every step copies its inputs from pinned host memory and its results (O, LSE, dQ, dK,
@@ -304,11 +315,7 @@ def run_native(args):
 
     e2e_run(3)
     barrier()
-    e2e_ms = e2e_run(E) / E
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_run(E) / E, dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     binding.device_status(stream)
@@ -347,7 +354,7 @@ def run_native(args):
         "fwd_frac_of_peak": round(fwd_tf / peak, 4), "bwd_frac_of_peak": round(fb / (bwd_ms * 1e-3) / 1e12 / peak, 4),
         "kernel_ms": {"fwd": round(fwd_ms, 4), "bwd_preprocess": round(pre_ms, 4), "bwd_main": round(main_ms, 4),
                       "bwd_dq_convert": round(conv_ms, 4)},
-        "e2e": {"value": round((ff + fb) * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_throughput(ff + fb, world, e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "steps": E, "pipelining": "copy-in, compute and copy-out streams, double-buffered device buffers"},
         "gpu_launches": 4 * K,

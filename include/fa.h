@@ -65,7 +65,7 @@ enum { FA_BRANCH_RM = 0, FA_BRANCH_BETA = 1, FA_BRANCH_ZERO = 2 };
  * "watch the max/min of the softmax input").  Each pointer is a device array
  * of B*H*N entries or NULL (not written).
  *   row_max_raw : rm, the largest visible raw score q.k (before scale)
- *   row_ties    : rs, how many visible keys reach rm exactly (FP32 equality)
+ *   row_ties    : rs, how many visible keys reach rm exactly (FP32 equality), all modes
  *   row_branch  : which shift the stabilised rule chose (FA_BRANCH_*); 0 in plain mode
  *   row_ones    : how many visible BF16 P~ entries of the row were exactly 1.0
  */
@@ -85,7 +85,11 @@ typedef struct {
  *             1 = stabilised shift [ijyty §4.1] with a running tie count over
  *                 all visible keys seen so far (m = beta*rm if rm > 0 and the
  *                 maximum repeats, 0 if rm < 0 and it repeats, else rm);
- *   beta    : shift factor for stable = 1; finite and >= 1 (ignored when stable = 0)
+ *             2 = the block-local reading of [ijyty §4.2]: each block of 128
+ *                 keys applies the same rule to its own max and tie count, and
+ *                 the row keeps the largest shift seen so far (depends on the
+ *                 block width; row_branch reports the block that set the shift);
+ *   beta    : shift factor for stable = 1, 2; finite and >= 1 (ignored when stable = 0)
  *   stats   : optional per-row statistics (NULL = none)
  * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA.
  */

@@ -99,7 +99,10 @@ __device__ __forceinline__ void ld_row32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-template <int D, bool kStable, bool kStats>
+// kStable: 0 = plain shift (running max); 1 = stabilised shift on the running (max, count)
+// of the row; 2 = block-local reading: each key block's own (max, count) picks a shift by
+// the same rule and the row keeps the largest shift seen so far.
+template <int D, int kStable, bool kStats>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -278,15 +281,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mx1 = max3f(mx1, sv[kBlockN - 2], sv[kBlockN - 1]);
       const float bm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       float m_new;
-      if constexpr (kStable || kStats) {
+      int bc = 0;
+      if constexpr (kStable != 0 || kStats) {
         // running (max, count) merge: rs' = [rm == rm'] rs + [bm == rm'] bc.  The block's
-        // count only matters when bm reaches the running max, so a warp whose rows all
-        // have bm < rm skips counting.
-        int bc = 0;
-        if (__any_sync(0xffffffffu, bm >= rm)) {
+        // count only matters when bm reaches the running max (or, block-locally, always),
+        // so a warp whose rows all have bm < rm skips counting.
+        if (kStable == 2 || __any_sync(0xffffffffu, bm >= rm)) {
+          // each equality gives an all-ones mask (-1); two masks per three-input add
+          uint32_t neg0 = 0, neg1 = 0;
 #pragma unroll
-          for (int i = 0; i < kBlockN; ++i) bc += (sv[i] == bm) ? 1 : 0;
-          bc = (bm == -INFINITY) ? 0 : bc;
+          for (int i = 0; i < kBlockN; i += 4) {
+            neg0 += eq_mask(sv[i], bm) + eq_mask(sv[i + 1], bm);
+            neg1 += eq_mask(sv[i + 2], bm) + eq_mask(sv[i + 3], bm);
+          }
+          bc = (bm == -INFINITY) ? 0 : -(int)(neg0 + neg1);
         }
         const float rm_new = fmaxf(rm, bm);
         rs = ((rm == rm_new) ? rs : 0) + ((bm == rm_new) ? bc : 0);
@@ -294,11 +302,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         rm = fmaxf(rm, bm);
       }
-      if constexpr (kStable) {
+      if constexpr (kStable == 1) {
         const bool rep = rs > 1;
         const bool pos = rep && (rm > 0.f), neg = rep && (rm < 0.f);
         m_new = pos ? p.beta * rm : (neg ? 0.f : rm);
         branch = pos ? 1 : (neg ? 2 : 0);
+      } else if constexpr (kStable == 2) {
+        const bool rep = bc > 1;
+        const bool pos = rep && (bm > 0.f), neg = rep && (bm < 0.f);
+        const float mb = pos ? p.beta * bm : (neg ? 0.f : bm);
+        const int brb = pos ? 1 : (neg ? 2 : 0);
+        branch = (mb >= m) ? brb : branch;   // branch of the block that set the shift
+        m_new = fmaxf(m, mb);
       } else {
         m_new = rm;
       }
@@ -407,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <int D, bool kStable, bool kStats>
+template <int D, int kStable, bool kStats>
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::fwd::Params& p,
                cudaStream_t stream) {
   using C = fa::fwd::Cfg<D>;
@@ -421,10 +436,11 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
 }
 
 template <int D>
-int dispatch_fwd(bool stable, bool stats, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+int dispatch_fwd(int stable, bool stats, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const fa::fwd::Params& p, cudaStream_t s) {
-  if (stable) return stats ? launch_fwd<D, true, true>(tq, tk, tv, p, s) : launch_fwd<D, true, false>(tq, tk, tv, p, s);
-  return stats ? launch_fwd<D, false, true>(tq, tk, tv, p, s) : launch_fwd<D, false, false>(tq, tk, tv, p, s);
+  if (stable == 2) return stats ? launch_fwd<D, 2, true>(tq, tk, tv, p, s) : launch_fwd<D, 2, false>(tq, tk, tv, p, s);
+  if (stable == 1) return stats ? launch_fwd<D, 1, true>(tq, tk, tv, p, s) : launch_fwd<D, 1, false>(tq, tk, tv, p, s);
+  return stats ? launch_fwd<D, 0, true>(tq, tk, tv, p, s) : launch_fwd<D, 0, false>(tq, tk, tv, p, s);
 }
 
 }  // namespace
@@ -439,7 +455,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     return rc;
   if (!lse) return set_error(FA_ERR_INVALID_ARG, "lse is NULL");
   if (!(scale > 0.f) || !isfinite(scale)) return set_error(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
-  if (stable != 0 && stable != 1) return set_error(FA_ERR_INVALID_ARG, "stable must be 0 or 1 (got %d)", stable);
+  if (stable < 0 || stable > 2) return set_error(FA_ERR_INVALID_ARG, "stable must be 0, 1 or 2 (got %d)", stable);
   if (stable && (!isfinite(beta) || beta < 1.f)) return set_error(FA_ERR_INVALID_ARG, "beta must be finite and >= 1");
   fwd::Params p{};
   p.o = static_cast<__nv_bfloat16*>(o);
@@ -466,6 +482,6 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
       (rc = make_tmap_bhnd(&tv, v, B * H, N, d, fwd::kBlockN)))
     return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? dispatch_fwd<64>(stable != 0, want_stats, tq, tk, tv, p, s)
-                 : dispatch_fwd<128>(stable != 0, want_stats, tq, tk, tv, p, s);
+  return d == 64 ? dispatch_fwd<64>(stable, want_stats, tq, tk, tv, p, s)
+                 : dispatch_fwd<128>(stable, want_stats, tq, tk, tv, p, s);
 }

@@ -291,6 +291,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 0xFFFFFFFF if a == b else 0 (one instruction; sums of these masks count equalities).
+__device__ __forceinline__ uint32_t eq_mask(float a, float b) {
+  uint32_t m;
+  asm("set.eq.u32.f32 %0, %1, %2;" : "=r"(m) : "f"(a), "f"(b));
+  return m;
+}
+
 // Three-input maximum (sm_100+).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;

@@ -66,7 +66,8 @@ def test_invalid_arguments_fail_before_touching_the_gpu(lib):
     assert _fwd(lib, good, good, good, good, None) == binding.FA_ERR_INVALID_ARG
     assert _fwd(lib, good, good, good, good, good, scale=float("nan")) == binding.FA_ERR_INVALID_ARG
     assert _fwd(lib, good, good, good, good, good, scale=0.0) == binding.FA_ERR_INVALID_ARG
-    assert _fwd(lib, good, good, good, good, good, stable=2) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, good, stable=3) == binding.FA_ERR_INVALID_ARG
+    assert _fwd(lib, good, good, good, good, good, stable=-1) == binding.FA_ERR_INVALID_ARG
     assert _fwd(lib, good, good, good, good, good, beta=0.9) == binding.FA_ERR_INVALID_ARG
     assert _fwd(lib, good, good, good, good, good, beta=float("inf")) == binding.FA_ERR_INVALID_ARG
 

@@ -129,3 +129,28 @@ def test_invalid_arguments_rejected_on_device():
     assert binding.fa_fwd(q, k, v, o, lse, True, 0.125, 1, 0.5) == binding.FA_ERR_INVALID_ARG
     assert binding.fa_fwd(q, k, v, o, lse, True, 0.125, 3, 1.25) == binding.FA_ERR_INVALID_ARG
     assert binding.fa_device_status() == binding.FA_OK
+
+
+@pytest.mark.parametrize("N", [128, 300, 1024])
+def test_block_local_variant_matches_emulation(N):
+    # stable = 2: each 128-key block applies the rule to its own (max, count); on dyadic
+    # inputs the per-row state, the branch of the block that set the shift and the
+    # exact-1.0 counts equal the BF16 emulation's
+    w = inputs.tiny_ties(N=N, H=2)
+    o, lse, st = run_fwd(w, 2)
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=2, beta=w.beta, block_n=128)
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=0)
+    assert_close_bf16("o", o, ref["o"])
+    assert_lse(lse, ref["lse"])
+    np.testing.assert_array_equal(st["row_max_raw"].cpu().numpy().astype(np.float64), ref["rm"])
+    np.testing.assert_array_equal(st["row_ties"].cpu().numpy(), ref["rs"])
+    np.testing.assert_array_equal(st["row_branch"].cpu().numpy(), em["branch"])
+    np.testing.assert_array_equal(st["row_ones"].cpu().numpy(), em["ones"])
+
+
+def test_block_local_variant_large_random():
+    w = inputs.gpt2_medium_sink(B=2, H=4, N=1024)
+    o, lse = run_fwd(w, 2, stats=False)
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=0)
+    assert_close_bf16("o", o, ref["o"])
+    assert_lse(lse, ref["lse"])
