@@ -14,11 +14,14 @@
 // P~V accumulate in FP32 (TMEM), the softmax runs in FP32, P~ is rounded to BF16
 // (round-to-nearest-even) for the P~V product.
 //
-// CTA organisation (one CTA = two 128-row query tiles of one (b, h)):
-//   warps 0-3  softmax warpgroup for tile 0 (thread = one query row = one TMEM lane)
-//   warps 4-7  softmax warpgroup for tile 1
-//   warp  8    MMA issuer (one elected thread)
-//   warp  9    TMA producer (one elected thread)
+// CTA organisation (one CTA = two 128-row query tiles of one (b, h)), 512 threads:
+//   warps 0-3   softmax warpgroup for tile 0 (thread = one query row = one TMEM lane)
+//   warps 4-7   softmax warpgroup for tile 1
+//   warps 8-11  correction warpgroup: O <- alpha O between P~V products, then O / l
+//   warp  12    MMA issuer (one elected thread)
+//   warp  13    TMA producer (one elected thread)
+// Registers are rebalanced after the launch (setmaxnreg): softmax threads hold a whole
+// 128-column row of S, the others need few.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1; the BF16 P~ of a tile is written
 // over the first 64 columns of its S (each thread has read its own S row first)
 // and fed to the P~V MMA straight from TMEM.
@@ -35,9 +38,15 @@ namespace fwd {
 constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;   // keys per block
 constexpr int kTiles = 2;      // query tiles per CTA
-constexpr int kThreads = 320;  // 10 warps
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kThreads = 512;  // 16 warps
+constexpr int kMmaWarp = 12;
+constexpr int kLoadWarp = 13;  // warps 14-15 only take part in set-up and teardown
+// Per-thread register budgets after the launch (setmaxnreg); the launch gives every thread
+// kRegLaunch registers and the split below must not exceed 512 * kRegLaunch.
+constexpr int kRegLaunch = 128;
+constexpr int kRegSoftmax = 184, kRegCorr = 80, kRegOther = 56;
+static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther <= kThreads * kRegLaunch,
+              "register split exceeds the launch allocation");
 
 template <int D>
 struct Cfg {
@@ -73,7 +82,10 @@ struct Shared {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t s_full[kTiles], p_ready[kTiles], pv_done[kTiles];
+  uint64_t alpha_ready[kTiles], o_ready[kTiles], l_ready[kTiles];
   uint64_t mma_done;
+  float alpha[kTiles][kBlockM];  // correction factor of each row for the current block
+  float lfin[kTiles][kBlockM];   // final row sums for the epilogue
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -132,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.s_full[t], 1);
       mbar_init(&sh.p_ready[t], kBlockM);
       mbar_init(&sh.pv_done[t], 1);
+      mbar_init(&sh.alpha_ready[t], kBlockM);
+      mbar_init(&sh.o_ready[t], kBlockM);
+      mbar_init(&sh.l_ready[t], kBlockM);
     }
     mbar_init(&sh.mma_done, 1);
     fence_barrier_init();
@@ -144,7 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
-
+  // Roles by warpgroup; each branch first rebalances its registers (setmaxnreg) so the
+  // softmax warpgroups can hold a 128-column row of S each.
+  if (warp >= 12) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther));
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
@@ -228,6 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kTiles; ++t) {
           if (j > 0 && j - 1 < nb[t]) {
             if (!(ok = mbar_wait(&sh.p_ready[t], (j - 1) & 1, abort_flag, p.status))) break;
+            // O_t must carry block j-1's correction (applied by the correction warpgroup)
+            if (j - 1 > 0 && !(ok = mbar_wait(&sh.o_ready[t], (j - 2) & 1, abort_flag, p.status))) break;
             tc_fence_after();
             issue_pv(t, sp, j - 1);
           }
@@ -241,15 +261,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(&sh.mma_done);
       mbar_wait(&sh.mma_done, 0, abort_flag, p.status);
     }
-  } else {
+  }
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warpgroups
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
     const int t = warp / 4;                      // tile
     const int lane_base = (warp % 4) * 32;       // TMEM lane quarter of this warp
     const int r = lane_base + (threadIdx.x % 32);  // row within the tile
     const int nb = (t == 0) ? nb0 : nb1;
     const int row = qb * (kTiles * kBlockM) + t * kBlockM + r;
     const uint32_t tS = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1) + ((uint32_t)lane_base << 16);
-    const uint32_t tO = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1) + ((uint32_t)lane_base << 16);
     const float c = p.scale_log2;
     float rm = -INFINITY, m = -INFINITY, l = 0.f;
     int rs = 0, ones = 0;
@@ -318,6 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_new = rm;
       }
       const float alpha = ex2_approx((m - m_new) * c);  // 0 on the first block (m = -inf)
+      if (j > 0) {
+        // hand the row's correction factor to the correction warpgroup right away
+        sh.alpha[t][r] = alpha;
+        mbar_arrive(&sh.alpha_ready[t]);
+      }
       const float nmc = -m_new * c;
       uint32_t pk[kBlockN / 2];
       float sum0 = 0.f, sum1 = 0.f;
@@ -347,37 +373,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tmem_st_wait();
-      // rescale O by alpha once the previous P~V has landed (skip when the whole warp has alpha == 1)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        if (!(ok = mbar_wait(&sh.pv_done[t], (j - 1) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t w[32];
-          tmem_ld32(tO + c0, w);
-          tmem_ld_wait();
-          reg_fence(w);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float a0, a1;
-            mul2(a0, a1, __uint_as_float(w[i]), __uint_as_float(w[i + 1]), alpha, alpha);
-            w[i] = __float_as_uint(a0);
-            w[i + 1] = __float_as_uint(a1);
-          }
-          tmem_st32(tO + c0, w);
-        }
-        tmem_st_wait();
-      }
       tc_fence_before();
       mbar_arrive(&sh.p_ready[t]);
       m = m_new;
     }
-    // ------------------------------------------------------------ epilogue
-    if (ok && nb > 0 && mbar_wait(&sh.pv_done[t], (nb - 1) & 1, abort_flag, p.status)) {
+    // ------------------------------------------------------------ row results
+    if (ok && nb > 0) {
+      sh.lfin[t][r] = l;
+      mbar_arrive(&sh.l_ready[t]);
+      if (row < p.N) {
+        const size_t srow = (size_t)bh * p.N + row;
+        p.lse[srow] = m * p.scale + logf(l);
+        if constexpr (kStats) {
+          if (p.stat_rm) p.stat_rm[srow] = rm;
+          if (p.stat_rs) p.stat_rs[srow] = rs;
+          if (p.stat_branch) p.stat_branch[srow] = (int8_t)branch;
+          if (p.stat_ones) p.stat_ones[srow] = ones;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ correction warpgroup
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCorr));
+    // O_t <- alpha O_t between P~V products (ijyty.com §2.1, O = diag(exp(m_prev - m)) O_prev + P~V),
+    // then the epilogue O = O / l.  Thread = row of the lane quarter, for both tiles.
+    const int lane_base = (warp % 4) * 32;
+    const int r = lane_base + (threadIdx.x % 32);
+    const int nb[2] = {nb0, nb1};
+    bool ok = true;
+    for (int j = 1; ok && j < nbmax; ++j) {
+      for (int t = 0; t < kTiles; ++t) {
+        if (j >= nb[t]) continue;
+        if (!(ok = mbar_wait(&sh.alpha_ready[t], (j - 1) & 1, abort_flag, p.status))) break;
+        const float alpha = sh.alpha[t][r];
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // the previous P~V of this tile has landed (its S_j commit already implies it)
+          if (!(ok = mbar_wait(&sh.pv_done[t], (j - 1) & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          const uint32_t tO = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1) + ((uint32_t)lane_base << 16);
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t w[32];
+            tmem_ld32(tO + c0, w);
+            tmem_ld_wait();
+            reg_fence(w);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float a0, a1;
+              mul2(a0, a1, __uint_as_float(w[i]), __uint_as_float(w[i + 1]), alpha, alpha);
+              w[i] = __float_as_uint(a0);
+              w[i + 1] = __float_as_uint(a1);
+            }
+            tmem_st32(tO + c0, w);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(&sh.o_ready[t]);
+      }
+    }
+    // ------------------------------------------------------------ epilogue: O = O / l -> BF16
+    for (int t = 0; ok && t < kTiles; ++t) {
+      if (nb[t] == 0) continue;
+      if (!(ok = mbar_wait(&sh.pv_done[t], (nb[t] - 1) & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.l_ready[t], 0, abort_flag, p.status))) break;
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = 1.f / sh.lfin[t][r];
+      const int row = qb * (kTiles * kBlockM) + t * kBlockM + r;
       const bool valid = row < p.N;
       const size_t orow = ((size_t)bh * p.N + (valid ? row : 0)) * D;
+      const uint32_t tO = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1) + ((uint32_t)lane_base << 16);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t w[32];
@@ -393,16 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4* dst = reinterpret_cast<uint4*>(p.o + orow + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
-        }
-      }
-      if (valid) {
-        const size_t srow = (size_t)bh * p.N + row;
-        p.lse[srow] = m * p.scale + logf(l);
-        if constexpr (kStats) {
-          if (p.stat_rm) p.stat_rm[srow] = rm;
-          if (p.stat_rs) p.stat_rs[srow] = rs;
-          if (p.stat_branch) p.stat_branch[srow] = (int8_t)branch;
-          if (p.stat_ones) p.stat_ones[srow] = ones;
         }
       }
     }
@@ -430,6 +485,14 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   int rc = fa::check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                           "cudaFuncSetAttribute(fwd)");
   if (rc) return rc;
+  // setmaxnreg.inc waits until the block's launch registers can cover the new split: refuse
+  // to launch a build whose launch allocation is smaller than the split needs
+  cudaFuncAttributes attr;
+  if ((rc = fa::check_cuda(cudaFuncGetAttributes(&attr, kern), "cudaFuncGetAttributes(fwd)"))) return rc;
+  constexpr int kSplit = 2 * 128 * fa::fwd::kRegSoftmax + 128 * fa::fwd::kRegCorr + 128 * fa::fwd::kRegOther;
+  if (attr.numRegs * fa::fwd::kThreads < kSplit)
+    return fa::set_error(FA_ERR_CUDA, "forward kernel built with %d registers/thread; its register split needs %d",
+                         attr.numRegs, (kSplit + fa::fwd::kThreads - 1) / fa::fwd::kThreads);
   const dim3 grid((unsigned)(p.n_qblocks * p.BH));
   kern<<<grid, fa::fwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return fa::check_cuda(cudaGetLastError(), "launch fa_fwd_kernel");
