@@ -5,7 +5,7 @@ the objects link into one shared library with the CUDA runtime linked
 statically, so loading the library needs no GPU and no libcuda (the driver's
 tensor-map encoder is looked up at run time).
 
-    python -m numerics_tcgen05_tmem_gb300.build [--debug-bounds]
+    python -m numerics_tcgen05_tmem_gb300.build [--testhooks]
 """
 from __future__ import annotations
 
@@ -20,6 +20,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfa.so")
+# Test-only build: FA_TEST_HOOKS compiles in the failure-injection hook and waits give up
+# after 100 ms.  Never loaded by the binding, the benchmark or the smoke check.
+LIB_TESTHOOKS = os.path.join(BUILD, "testhooks", "libfa_testhooks.so")
+TESTHOOKS_FLAGS = ["-DFA_TEST_HOOKS=1", "-DFA_WAIT_TIMEOUT_NS=100000000ull"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -34,28 +38,32 @@ def _sources():
     return sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _needs_rebuild(extra_flags) -> bool:
-    if not os.path.exists(LIB):
+def _needs_rebuild(extra_flags, lib=LIB, objdir=BUILD) -> bool:
+    if not os.path.exists(lib):
         return True
-    stamp = os.path.join(BUILD, "flags.txt")
+    stamp = os.path.join(objdir, "flags.txt")
     if not os.path.exists(stamp) or open(stamp).read() != " ".join(extra_flags):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(HERE, "..", "include", "fa.h")]
     return any(os.path.getmtime(p) > t for p in deps if os.path.exists(p))
 
 
-def build(force: bool = False, debug_bounds: bool = False, verbose: bool = False) -> str:
-    extra = ["-DFA_DEBUG_BOUNDS=1"] if debug_bounds else []
-    if not force and not _needs_rebuild(extra):
-        return LIB
+def build(force: bool = False, verbose: bool = False, testhooks: bool = False) -> str:
+    extra = []
+    lib, objdir = LIB, BUILD
+    if testhooks:
+        extra = extra + TESTHOOKS_FLAGS
+        lib, objdir = LIB_TESTHOOKS, os.path.dirname(LIB_TESTHOOKS)
+    if not force and not _needs_rebuild(extra, lib, objdir):
+        return lib
     nvcc = nvcc_path()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(objdir, exist_ok=True)
     common = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", CSRC,
                      "-I", os.path.join(HERE, "..", "include")] + extra
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src[:-3] + ".o")
+        obj = os.path.join(objdir, src[:-3] + ".o")
         cmd = [nvcc] + common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,24 +75,24 @@ def build(force: bool = False, debug_bounds: bool = False, verbose: bool = False
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    with open(os.path.join(BUILD, "flags.txt"), "w") as f:
+    os.replace(tmp, lib)
+    with open(os.path.join(objdir, "flags.txt"), "w") as f:
         f.write(" ".join(extra))
-    return LIB
+    return lib
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
-    ap.add_argument("--debug-bounds", action="store_true")
+    ap.add_argument("--testhooks", action="store_true", help="build the failure-injection test library")
     ap.add_argument("-v", "--verbose", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, debug_bounds=a.debug_bounds, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, testhooks=a.testhooks))
 
 
 if __name__ == "__main__":

@@ -323,7 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_commit(&sh.mma_done);
-      mbar_wait(&sh.mma_done, 0, abort_flag, p.status);
+      {
+        // MMAs still in flight must finish before TMEM is released, even after an abort
+        volatile uint32_t ignore_abort = 0;
+        mbar_wait(&sh.mma_done, 0, &ignore_abort, p.status);
+      }
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ P^T / dS^T warpgroups

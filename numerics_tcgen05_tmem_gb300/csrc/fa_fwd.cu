@@ -28,6 +28,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 
 #include "fa_host.h"
 #include "sm103.cuh"
@@ -76,6 +77,7 @@ struct Params {
   float scale;
   float scale_log2;  // scale * log2(e)
   float beta;
+  int inject_stall;  // test builds only (FA_TEST_HOOKS): make the MMA warp's first wait run out
 };
 
 struct Shared {
@@ -84,6 +86,7 @@ struct Shared {
   uint64_t s_full[kTiles], p_ready[kTiles], pv_done[kTiles];
   uint64_t alpha_ready[kTiles], o_ready[kTiles], l_ready[kTiles];
   uint64_t mma_done;
+  uint64_t never;  // test builds only: a barrier nothing arrives on
   float alpha[kTiles][kBlockM];  // correction factor of each row for the current block
   float lfin[kTiles][kBlockM];   // final row sums for the epilogue
   uint32_t tmem_base;
@@ -149,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.l_ready[t], kBlockM);
     }
     mbar_init(&sh.mma_done, 1);
+    mbar_init(&sh.never, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -208,6 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sV = smem_u32(smem + C::kVOff);
       const int nb[2] = {nb0, nb1};
       bool ok = mbar_wait(&sh.q_full, 0, abort_flag, p.status);
+#ifdef FA_TEST_HOOKS
+      // failure-detection test: wait on a barrier nothing arrives on; the bounded wait runs
+      // out, raises the CTA's abort flag and records a timeout, and every warp unwinds
+      if (p.inject_stall) ok = ok && mbar_wait(&sh.never, 0, abort_flag, p.status);
+#endif
       tc_fence_after();
       // S_t = Q_t K_j^T over D/16 k-steps (K-major SW128 operands, 16 KB per 64 columns)
       auto issue_s = [&](int t, int s) {
@@ -259,7 +268,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every MMA issued above has completed before TMEM is released
       tc_commit(&sh.mma_done);
-      mbar_wait(&sh.mma_done, 0, abort_flag, p.status);
+      {
+        // MMAs still in flight must finish before TMEM is released, even after an abort
+        volatile uint32_t ignore_abort = 0;
+        mbar_wait(&sh.mma_done, 0, &ignore_abort, p.status);
+      }
     }
   }
   } else if (warp < 8) {
@@ -540,6 +553,10 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.beta = beta;
+#ifdef FA_TEST_HOOKS
+  const char* inject = getenv("FA_TEST_INJECT_STALL");
+  p.inject_stall = (inject && inject[0] == '1') ? 1 : 0;
+#endif
   CUtensorMap tq, tk, tv;
   if ((rc = make_tmap_bhnd(&tq, q, B * H, N, d, fwd::kBlockM)) || (rc = make_tmap_bhnd(&tk, k, B * H, N, d, fwd::kBlockN)) ||
       (rc = make_tmap_bhnd(&tv, v, B * H, N, d, fwd::kBlockN)))

@@ -1,0 +1,65 @@
+"""Failure detection on the GPU without a fault: a bounded wait that runs out.
+
+Every mbarrier wait in the kernels gives up after a time limit, raises the CTA's
+abort flag, records FA_ERR_TIMEOUT in the device status word and lets every warp
+unwind (in-flight copies land, TMEM is freed).  A test build of the library
+(FA_TEST_HOOKS, 100 ms limit) can make the MMA warp wait on a barrier that nothing
+arrives on.  The call must report the timeout through fa_device_status, and the
+same CUDA context must then compute correct results.
+"""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from numerics_tcgen05_tmem_gb300 import binding, build, inputs
+from oracle import attention as A
+from tests._parity import assert_close_bf16, require_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hooks_lib():
+    require_gpu()
+    path = build.build(testhooks=True)
+    lib = ctypes.CDLL(path)
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, vp, vp]
+    lib.fa_fwd.restype = ci
+    lib.fa_device_status.argtypes = [vp]
+    lib.fa_device_status.restype = ci
+    lib.fa_last_error.restype = ctypes.c_char_p
+    return lib
+
+
+def _fwd(lib, w, q, k, v, o, lse):
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    B, H, N, d = q.shape
+    return lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                      int(w.causal), w.scale, 1, w.beta, None, stream)
+
+
+def test_wait_that_runs_out_reports_timeout_and_context_stays_usable(hooks_lib, monkeypatch):
+    w = inputs.gpt2_small(B=1, H=4, N=512)
+    q, k, v, _ = to_dev(w)
+    o = torch.zeros_like(q)
+    lse = torch.zeros(q.shape[:3], device=q.device, dtype=torch.float32)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    monkeypatch.setenv("FA_TEST_INJECT_STALL", "1")
+    assert _fwd(hooks_lib, w, q, k, v, o, lse) == binding.FA_OK      # the launch itself is fine
+    assert hooks_lib.fa_device_status(stream) == binding.FA_ERR_TIMEOUT
+    assert b"timed out" in hooks_lib.fa_last_error()
+    assert hooks_lib.fa_device_status(stream) == binding.FA_OK       # reading clears the word
+    # same context, no injection: a normal, correct result
+    monkeypatch.setenv("FA_TEST_INJECT_STALL", "0")
+    assert _fwd(hooks_lib, w, q, k, v, o, lse) == binding.FA_OK
+    assert hooks_lib.fa_device_status(stream) == binding.FA_OK
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, beta=w.beta)
+    assert_close_bf16("o", o, ref["o"])
+    # and the product library in the same process is unaffected
+    o2, lse2 = binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=1)
+    binding.device_status()
+    assert torch.equal(o2, o)
