@@ -351,24 +351,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(&sh.s_full, it & 1, abort_flag, p.status))) break;
       tc_fence_after();
       // P^T = exp2(S^T c - lse_q log2 e); padded queries carry lse = +inf -> 0
+      // this warpgroup's 64 columns of the row in one round trip
+      uint32_t w[64];
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(w));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(w + 32));
+      tmem_ld_wait();
+      reg_fence(w);
       float pr[64];
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t w[32];
-        tmem_ld32(tS + c0, w);
-        tmem_ld_wait();
-        reg_fence(w);
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 l4 = lse4[(c0 + i) / 4];
-          float x0, x1, x2, x3;
-          fma2(x0, x1, __uint_as_float(w[i + 0]), __uint_as_float(w[i + 1]), c, c, -l4.x, -l4.y);
-          fma2(x2, x3, __uint_as_float(w[i + 2]), __uint_as_float(w[i + 3]), c, c, -l4.z, -l4.w);
-          pr[c0 + i + 0] = ex2_approx(x0);
-          pr[c0 + i + 1] = ex2_approx(x1);
-          pr[c0 + i + 2] = ex2_approx(x2);
-          pr[c0 + i + 3] = ex2_approx(x3);
-        }
+      for (int i = 0; i < 64; i += 4) {
+        const float4 l4 = lse4[i / 4];
+        float x0, x1, x2, x3;
+        fma2(x0, x1, __uint_as_float(w[i + 0]), __uint_as_float(w[i + 1]), c, c, -l4.x, -l4.y);
+        fma2(x2, x3, __uint_as_float(w[i + 2]), __uint_as_float(w[i + 3]), c, c, -l4.z, -l4.w);
+        pr[i + 0] = ex2_approx(x0);
+        pr[i + 1] = ex2_approx(x1);
+        pr[i + 2] = ex2_approx(x2);
+        pr[i + 3] = ex2_approx(x3);
       }
       if (diag) {
         // query column 64h + j is visible to key row r iff 64h + j >= r

@@ -104,16 +104,6 @@ __device__ __forceinline__ int tile_blocks(const Params& p, int qb, int t) {
   return min(nk, last + 1);
 }
 
-// Load 32 consecutive FP32 columns of this thread's TMEM lane into v[off..off+31].
-__device__ __forceinline__ void ld_row32(uint32_t taddr, float* v) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
-  tmem_ld_wait();
-  reg_fence(r);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // kStable: 0 = plain shift (running max); 1 = stabilised shift on the running (max, count)
 // of the row; 2 = block-local reading: each key block's own (max, count) picks a shift by
 // the same rule and the row keeps the largest shift seen so far.
@@ -292,9 +282,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nb; ++j) {
       if (!(ok = mbar_wait(&sh.s_full[t], j & 1, abort_flag, p.status))) break;
       tc_fence_after();
+      // the whole 128-column row in one round trip: four loads, one wait
+      uint32_t raw[kBlockN];
+#pragma unroll
+      for (int c0 = 0; c0 < kBlockN; c0 += 32) tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(raw + c0));
+      tmem_ld_wait();
+      reg_fence(raw);
       float sv[kBlockN];
 #pragma unroll
-      for (int c0 = 0; c0 < kBlockN; c0 += 32) ld_row32(tS + c0, sv + c0);
+      for (int i = 0; i < kBlockN; ++i) sv[i] = __uint_as_float(raw[i]);
       // mask: keys past N, and keys after the query on the causal diagonal
       const int col0 = j * kBlockN;
       const int lim = p.causal ? min(p.N - col0, row - col0 + 1) : (p.N - col0);
