@@ -18,8 +18,9 @@
 //   warps 0-7  two "softmax" warpgroups; thread = key row (TMEM lane) of the tile,
 //              warpgroup h takes query columns [64h, 64h+64):
 //              P^T = exp2(S^T c - lse_q log2 e) into TMEM (BF16) for the dV MMA,
-//              dS^T = P^T o (dP^T - delta_q) into shared memory (BF16, 128B swizzle)
-//              for the dK and dQ MMAs; finally warpgroup 0 writes dK, 1 writes dV.
+//              dS^T = P^T o (dP^T - delta_q) as BF16 into its dP^T columns of TMEM (the A
+//              operand of the dK MMA) and into shared memory (128B swizzle; the MN-major
+//              A operand of the dQ MMA); finally warpgroup 0 writes dK, 1 writes dV.
 //   warps 8-11 dQ warpgroup: thread = query row; loads each dQ tile from TMEM, hands
 //              the columns back, then reduces it into the FP32 dQ accumulator.
 //   warp  12   MMA issuer;  warp 13  TMA producer (Q, dO tiles and the per-tile
@@ -301,9 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dK += dS^T Q_i ;  dQ_i = dS K_j
         if (!(ok = mbar_wait(&sh.ds_ready, it & 1, abort_flag, p.status))) break;
         tc_fence_after();
+        // dS^T (BF16) sits in dP^T's columns 0-31 (queries 0-63) and 64-95 (queries 64-127);
+        // reading it from TMEM spares shared-memory bandwidth (dQ, issued next, overwrites
+        // those columns only after this MMA has read them: same-thread MMAs run in order)
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk)
-          mma_ss(tmem + C::kTmemDK, kmaj(sDS, kk), mnmaj(q, kk), C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::kTmemDK, tmem + C::kTmemDP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(q, kk),
+                 C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk)
           mma_ss(tmem + C::kTmemDQ, mnmaj(sDS, kk), mnmaj(sK, kk), C::kIdescQ, kk > 0);
@@ -395,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tDP + c0, w);
         tmem_ld_wait();
         reg_fence(w);
+        uint32_t dsk[16];  // this chunk's dS^T as BF16 pairs, also kept in TMEM for the dK MMA
         // row r of dS^T, 16-byte chunk g (8 queries) of this 64-query block, swizzled (g ^ r%8)
 #pragma unroll
         for (int gg = 0; gg < 4; ++gg) {
@@ -413,10 +419,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           mul2(g[6], g[7], g[6], g[7], pp[6], pp[7]);
           const uint4 v4 = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
                                       pack_bf16x2(g[6], g[7]));
+          dsk[4 * gg] = v4.x;
+          dsk[4 * gg + 1] = v4.y;
+          dsk[4 * gg + 2] = v4.z;
+          dsk[4 * gg + 3] = v4.w;
           const uint32_t chunk = (uint32_t)(c0 / 8 + gg);
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ sw) << 4)) = v4;
         }
+        // packed columns [c0/2, c0/2 + 16) of this warpgroup's dP^T region: their dP^T values
+        // (columns < c0 + 32) have already been read
+        __syncwarp();
+        tmem_st16(tDP + c0 / 2, dsk);
       }
+      tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(&sh.ds_ready);
