@@ -154,3 +154,26 @@ def test_block_local_variant_large_random():
     ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=0)
     assert_close_bf16("o", o, ref["o"])
     assert_lse(lse, ref["lse"])
+
+
+def test_zero_maximum_ties_keep_branch_zero():
+    # A zero query row scores 0 against every key: its maximum 0 repeats, which matches
+    # neither branch of the shift rule (rm > 0 or rm < 0), so m = 0, every visible P~ is
+    # exactly 1.0 and the output is the mean of the visible values.
+    w = inputs.random_case(1, 2, 200, 64, True, seed=77)
+    q = w.q.clone()
+    q[:, :, 5] = 0
+    q[:, :, 150] = 0
+    w = inputs.Workload("zero_rows", q, w.k, w.v, w.do, True, w.scale, 1, 1.25)
+    o, lse, st = run_fwd(w, 1)
+    ref = A.forward(w.q, w.k, w.v, w.scale, True, stable=1, beta=1.25)
+    assert_close_bf16("o", o, ref["o"])
+    assert_lse(lse, ref["lse"])
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, True, stable=1, beta=1.25, block_n=128)
+    for row in (5, 150):
+        assert np.all(ref["rm"][0, :, row] == 0) and np.all(ref["rs"][0, :, row] == row + 1)
+        np.testing.assert_array_equal(st["row_branch"][0, :, row].cpu().numpy(), [0, 0])
+        np.testing.assert_array_equal(st["row_ties"][0, :, row].cpu().numpy(), [row + 1] * 2)
+        np.testing.assert_array_equal(st["row_ones"][0, :, row].cpu().numpy(), em["ones"][0, :, row])
+        np.testing.assert_allclose(f64(o[0, :, row]), f64(w.v[0, :, :row + 1]).mean(axis=1), atol=1e-2)
+    assert np.all(em["ones"][0, :, 5] == 6)
