@@ -54,7 +54,8 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d not in {64, 128}) */
   FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see fa_last_error() */
   FA_ERR_TIMEOUT = 4,       /* (fa_device_status) a kernel's bounded wait ran out */
-  FA_ERR_DEVICE_BOUNDS = 5  /* (fa_device_status) a debug bounds check fired */
+  FA_ERR_DEVICE_BOUNDS = 5, /* (fa_device_status) a device-side layout check fired */
+  FA_WARN_NONFINITE = 6     /* (fa_device_status) an output (O, LSE, dQ, dK or dV) held NaN or Inf */
 } fa_status;
 
 /* Shift branch codes written to fa_row_stats.row_branch. */
@@ -68,12 +69,14 @@ enum { FA_BRANCH_RM = 0, FA_BRANCH_BETA = 1, FA_BRANCH_ZERO = 2 };
  *   row_ties    : rs, how many visible keys reach rm exactly (FP32 equality), all modes
  *   row_branch  : which shift the stabilised rule chose (FA_BRANCH_*); 0 in plain mode
  *   row_ones    : how many visible BF16 P~ entries of the row were exactly 1.0
+ *   row_min_raw : the smallest visible raw score of the row
  */
 typedef struct {
   float* row_max_raw;
   int32_t* row_ties;
   int8_t* row_branch;
   int32_t* row_ones;
+  float* row_min_raw;
 } fa_row_stats;
 
 /*
@@ -169,8 +172,11 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 
 /*
  * fa_device_status -- synchronise `stream`, then return and clear the current
- * device's status word: FA_OK, FA_ERR_TIMEOUT or FA_ERR_DEVICE_BOUNDS
- * (FA_ERR_CUDA if the synchronisation itself fails).
+ * device's status word: FA_OK, FA_ERR_TIMEOUT, FA_ERR_DEVICE_BOUNDS or
+ * FA_WARN_NONFINITE (in that order of precedence; FA_ERR_CUDA if the
+ * synchronisation itself fails).  FA_WARN_NONFINITE is the NaN monitor of
+ * [jsqmd §5] / [ijyty §7.1]: some output written since the last read held a
+ * NaN or an Inf (e.g. from non-finite inputs); the call itself completed.
  */
 int fa_device_status(void* stream);
 

@@ -21,6 +21,7 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_CUDA = 3
 FA_ERR_TIMEOUT = 4
 FA_ERR_DEVICE_BOUNDS = 5
+FA_WARN_NONFINITE = 6
 
 # every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_staged", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_device_status",
@@ -40,7 +41,8 @@ class FAError(RuntimeError):
 
 class RowStats(ctypes.Structure):
     _fields_ = [("row_max_raw", ctypes.c_void_p), ("row_ties", ctypes.c_void_p),
-                ("row_branch", ctypes.c_void_p), ("row_ones", ctypes.c_void_p)]
+                ("row_branch", ctypes.c_void_p), ("row_ones", ctypes.c_void_p),
+                ("row_min_raw", ctypes.c_void_p)]
 
 
 _lib = None
@@ -109,7 +111,7 @@ def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stable: int, beta: float
     st = None
     if stats is not None:
         st = RowStats(*(None if stats.get(n) is None else stats[n].data_ptr()
-                        for n in ("row_max_raw", "row_ties", "row_branch", "row_ones")))
+                        for n in ("row_max_raw", "row_ties", "row_branch", "row_ones", "row_min_raw")))
     return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
                          float(scale), int(stable), float(beta), ctypes.byref(st) if st is not None else None,
                          _stream(stream))
@@ -157,7 +159,8 @@ def forward(q, k, v, causal: bool = True, scale=None, stable: int = 1, beta: flo
         sd = {"row_max_raw": torch.empty((B, H, N), device=q.device, dtype=torch.float32),
               "row_ties": torch.empty((B, H, N), device=q.device, dtype=torch.int32),
               "row_branch": torch.empty((B, H, N), device=q.device, dtype=torch.int8),
-              "row_ones": torch.empty((B, H, N), device=q.device, dtype=torch.int32)}
+              "row_ones": torch.empty((B, H, N), device=q.device, dtype=torch.int32),
+              "row_min_raw": torch.empty((B, H, N), device=q.device, dtype=torch.float32)}
     _check(fa_fwd(q, k, v, o, lse, causal, scale, stable, beta, sd, stream))
     return (o, lse, sd) if stats else (o, lse)
 

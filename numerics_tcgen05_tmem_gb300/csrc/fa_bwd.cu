@@ -139,11 +139,20 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __
 // --------------------------------------------------------------------------- dQ convert
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict__ dq_acc,
                                                          __nv_bfloat16* __restrict__ dq, float scale,
-                                                         long long n8) {
+                                                         long long n8, uint32_t* status) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  const bool in = i < n8;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+  if (in) {
+    a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
+    b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
+  }
+  const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
+                         fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+  report_nonfinite(!(mx < INFINITY) || (a.x != a.x) || (a.y != a.y) || (a.z != a.z) || (a.w != a.w) ||
+                       (b.x != b.x) || (b.y != b.y) || (b.z != b.z) || (b.w != b.w),
+                   status);
+  if (!in) return;
   uint4 out;
   out.x = pack_bf16x2(a.x * scale, a.y * scale);
   out.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -453,8 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence(w);
         uint4 pkd[4];
         uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+        bool bad = false;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
+        for (int i = 0; i < 16; ++i) {
+          const float g0 = __uint_as_float(w[2 * i]) * mul, g1 = __uint_as_float(w[2 * i + 1]) * mul;
+          bad |= !(fabsf(g0) < INFINITY) || !(fabsf(g1) < INFINITY);
+          pw[i] = pack_bf16x2(g0, g1);
+        }
+        report_nonfinite(bad && valid, p.status);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(out + orow + c0);
 #pragma unroll
@@ -603,8 +618,10 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   }
   if (!(stages & FA_BWD_DQ_CONVERT)) return FA_OK;
   const long long n8 = rows * D / 8;
+  uint32_t* st_word = status_word ? status_word : device_status_word();
+  if (!st_word) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
   bwd::fa_bwd_dq_convert<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(sc.dq_acc, static_cast<__nv_bfloat16*>(dq),
-                                                                           scale, n8);
+                                                                           scale, n8, st_word);
   return check_cuda(cudaGetLastError(), "launch fa_bwd_dq_convert");
 }
 

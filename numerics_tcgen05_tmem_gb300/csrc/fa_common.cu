@@ -126,7 +126,8 @@ extern "C" int fa_device_status(void* stream) {
     if (rc) return rc;
   }
   if (v & fa::kDevTimeout) return fa::set_error(FA_ERR_TIMEOUT, "a kernel's bounded wait timed out");
-  if (v & fa::kDevBounds) return fa::set_error(FA_ERR_DEVICE_BOUNDS, "a device bounds check failed");
+  if (v & fa::kDevBounds) return fa::set_error(FA_ERR_DEVICE_BOUNDS, "a device-side layout check failed");
+  if (v & fa::kDevNonFinite) return fa::set_error(FA_WARN_NONFINITE, "an output held NaN or Inf");
   return FA_OK;
 }
 

@@ -45,7 +45,7 @@ constexpr int kLoadWarp = 13;  // warps 14-15 only take part in set-up and teard
 // Per-thread register budgets after the launch (setmaxnreg); the launch gives every thread
 // kRegLaunch registers and the split below must not exceed 512 * kRegLaunch.
 constexpr int kRegLaunch = 128;
-constexpr int kRegSoftmax = 184, kRegCorr = 80, kRegOther = 56;
+constexpr int kRegSoftmax = 176, kRegCorr = 96, kRegOther = 56;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther <= kThreads * kRegLaunch,
               "register split exceeds the launch allocation");
 
@@ -69,6 +69,7 @@ struct Params {
   int32_t* stat_rs;
   int8_t* stat_branch;
   int32_t* stat_ones;
+  float* stat_min;
   uint32_t* status;
   int N;
   int BH;
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1) + ((uint32_t)lane_base << 16);
     const float c = p.scale_log2;
     float rm = -INFINITY, m = -INFINITY, l = 0.f;
+    float rmin = INFINITY;  // smallest visible raw score (statistics only)
     int rs = 0, ones = 0;
     int branch = 0;
     bool ok = true;
@@ -310,6 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mx0 = max3f(mx0, sv[kBlockN - 4], sv[kBlockN - 3]);
       mx1 = max3f(mx1, sv[kBlockN - 2], sv[kBlockN - 1]);
       const float bm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      if constexpr (kStats) {
+        // masked entries hold -inf; they never count as the row's minimum
+        float mn0 = INFINITY, mn1 = INFINITY;
+#pragma unroll
+        for (int i = 0; i < kBlockN; i += 4) {
+          mn0 = min3f(mn0, sv[i] == -INFINITY ? INFINITY : sv[i], sv[i + 1] == -INFINITY ? INFINITY : sv[i + 1]);
+          mn1 = min3f(mn1, sv[i + 2] == -INFINITY ? INFINITY : sv[i + 2], sv[i + 3] == -INFINITY ? INFINITY : sv[i + 3]);
+        }
+        rmin = fminf(rmin, fminf(mn0, mn1));
+      }
       float m_new;
       int bc = 0;
       if constexpr (kStable != 0 || kStats) {
@@ -390,14 +402,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && nb > 0) {
       sh.lfin[t][r] = l;
       mbar_arrive(&sh.l_ready[t]);
+      const float lse_row = m * p.scale + logf(l);
+      report_nonfinite(row < p.N && !(fabsf(lse_row) < INFINITY), p.status);
       if (row < p.N) {
         const size_t srow = (size_t)bh * p.N + row;
-        p.lse[srow] = m * p.scale + logf(l);
+        p.lse[srow] = lse_row;
         if constexpr (kStats) {
           if (p.stat_rm) p.stat_rm[srow] = rm;
           if (p.stat_rs) p.stat_rs[srow] = rs;
           if (p.stat_branch) p.stat_branch[srow] = (int8_t)branch;
           if (p.stat_ones) p.stat_ones[srow] = ones;
+          if (p.stat_min) p.stat_min[srow] = rmin;
         }
       }
     }
@@ -460,9 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence(w);
         uint4 pkd[4];
         uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
+        bool bad = false;
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pw[i] = pack_bf16x2(__uint_as_float(w[2 * i]) * inv_l, __uint_as_float(w[2 * i + 1]) * inv_l);
+        for (int i = 0; i < 16; ++i) {
+          const float o0 = __uint_as_float(w[2 * i]) * inv_l, o1 = __uint_as_float(w[2 * i + 1]) * inv_l;
+          bad |= !(fabsf(o0) < INFINITY) || !(fabsf(o1) < INFINITY);
+          pw[i] = pack_bf16x2(o0, o1);
+        }
+        report_nonfinite(bad && valid, p.status);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + orow + c0);
 #pragma unroll
@@ -538,7 +558,8 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     p.stat_rs = stats->row_ties;
     p.stat_branch = stats->row_branch;
     p.stat_ones = stats->row_ones;
-    want_stats = p.stat_rm || p.stat_rs || p.stat_branch || p.stat_ones;
+    p.stat_min = stats->row_min_raw;
+    want_stats = p.stat_rm || p.stat_rs || p.stat_branch || p.stat_ones || p.stat_min;
   }
   p.status = device_status_word();
   if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");

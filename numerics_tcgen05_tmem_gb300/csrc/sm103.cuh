@@ -16,8 +16,22 @@ namespace fa {
 enum : uint32_t {
   kDevOk = 0,
   kDevTimeout = 1u << 0,   // a bounded wait on an mbarrier ran out
-  kDevBounds = 1u << 1,    // a debug bounds check failed
+  kDevBounds = 1u << 1,    // a device-side layout check failed
+  kDevNonFinite = 1u << 2, // an output value was NaN or Inf
 };
+
+// Record kDevNonFinite once per warp if any lane saw a non-finite output value.  All 32
+// lanes of the warp must call it (it votes across the warp).
+__device__ __forceinline__ void report_nonfinite(bool bad, uint32_t* status) {
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x % 32) == 0) atomicOr(status, kDevNonFinite);
+}
+
+// Three-input minimum (sm_100+).
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 // A wait gives up after this many nanoseconds of %globaltimer.
 #ifndef FA_WAIT_TIMEOUT_NS

@@ -95,6 +95,7 @@ def forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: float = 
       o   [B, H, N, d]  softmax(scale * q k^T) v
       lse [B, H, N]     logsumexp_j(scale * S_raw[i, j]) over visible j
       rm  [B, H, N]     raw row maximum;  rs: how often it occurs
+      rmin [B, H, N]    raw row minimum over visible keys (the monitor's softmax-input min)
       branch [B, H, N]  which shift the stabilised rule picks (0, 1, 2)
       m   [B, H, N]     the shift used (raw units)
     The outputs are computed with the shift the rule picks; o and lse do not
@@ -108,6 +109,7 @@ def forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: float = 
         "o": np.zeros((B, H, N, v.shape[-1])),
         "lse": np.zeros((B, H, N)),
         "rm": np.zeros((B, H, N)),
+        "rmin": np.zeros((B, H, N)),
         "rs": np.zeros((B, H, N), dtype=np.int64),
         "branch": np.zeros((B, H, N), dtype=np.int8),
         "m": np.zeros((B, H, N)),
@@ -126,6 +128,7 @@ def forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: float = 
                 out["o"][b, h, rows] = (e / l[:, None]) @ v[b, h]
                 out["lse"][b, h, rows] = shift + np.log(l)
                 out["rm"][b, h, rows] = rm
+                out["rmin"][b, h, rows] = np.where(vis, s_raw, np.inf).min(axis=1)
                 out["rs"][b, h, rows] = rs
                 out["branch"][b, h, rows] = br
                 out["m"][b, h, rows] = m

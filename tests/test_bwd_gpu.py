@@ -114,3 +114,18 @@ def test_invalid_workspace_rejected():
     rc = binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, None, True, w.scale, small)
     assert rc == binding.FA_ERR_INVALID_ARG
     assert binding.fa_device_status() == binding.FA_OK
+
+
+def test_nonfinite_gradients_are_reported():
+    w = inputs.random_case(1, 2, 256, 64, True, seed=4)
+    q, k, v, do = to_dev(w)
+    o, lse = binding.forward(q, k, v, causal=True, scale=w.scale)
+    binding.device_status()
+    do[0, 0, 200, 5] = float("nan")
+    ws = torch.empty(binding.fa_bwd_workspace_size(*q.shape), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    assert binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, None, True, w.scale, ws) == binding.FA_OK
+    assert binding.fa_device_status() == binding.FA_WARN_NONFINITE
+    do[0, 0, 200, 5] = 0.0
+    assert binding.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, None, True, w.scale, ws) == binding.FA_OK
+    assert binding.fa_device_status() == binding.FA_OK

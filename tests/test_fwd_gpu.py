@@ -177,3 +177,30 @@ def test_zero_maximum_ties_keep_branch_zero():
         np.testing.assert_array_equal(st["row_ones"][0, :, row].cpu().numpy(), em["ones"][0, :, row])
         np.testing.assert_allclose(f64(o[0, :, row]), f64(w.v[0, :, :row + 1]).mean(axis=1), atol=1e-2)
     assert np.all(em["ones"][0, :, 5] == 6)
+
+
+def test_row_minimum_statistic():
+    w = inputs.tiny_ties(N=300)
+    o, lse, st = run_fwd(w, 1)
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, beta=w.beta)
+    # dyadic inputs: FP32 scores are exact
+    np.testing.assert_array_equal(st["row_min_raw"].cpu().numpy().astype(np.float64), ref["rmin"])
+
+
+def test_nonfinite_outputs_are_reported():
+    # ijyty.com §7.1 / jsqmd.com §5 NaN monitor: an Inf in V reaches O; the call completes
+    # and fa_device_status reports FA_WARN_NONFINITE once, then the word is clear again
+    w = inputs.random_case(1, 2, 256, 64, True, seed=3)
+    q, k, v, do = to_dev(w)
+    v[0, 1, 7, 3] = float("inf")
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+    assert binding.fa_fwd(q, k, v, o, lse, True, w.scale, 1, 1.25) == binding.FA_OK
+    assert binding.fa_device_status() == binding.FA_WARN_NONFINITE
+    assert binding.fa_device_status() == binding.FA_OK
+    # the finite head is unaffected
+    ref = A.forward(w.q[:, :1], w.k[:, :1], w.v[:, :1], w.scale, True, stable=1)
+    assert_close_bf16("o", o[:, :1], ref["o"])
+    v[0, 1, 7, 3] = 0.0
+    assert binding.fa_fwd(q, k, v, o, lse, True, w.scale, 1, 1.25) == binding.FA_OK
+    assert binding.fa_device_status() == binding.FA_OK

@@ -238,3 +238,15 @@ def test_near_tie_is_undecidable():
     k[0, 0, 1, 5] += 1e-9 / q[0, 0, 1, 5]
     dec, _ = A.decidable_rows(q, k, False)
     assert not dec[1]
+
+
+def test_row_minimum_over_visible_keys():
+    # hand example: row 2 sees keys 0..2 (causal) with scores 3, -4, 7 -> min -4
+    q = np.array([[[[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]]]])
+    k = np.array([[[[3.0, 0.0], [0.0, -4.0], [4.0, 3.0]]]])
+    v = np.zeros((1, 1, 3, 2))
+    out = A.forward(q, k, v, 1.0, True)
+    assert out["rmin"][0, 0, 2] == -4.0 and out["rm"][0, 0, 2] == 7.0
+    assert out["rmin"][0, 0, 0] == 3.0        # only key 0 visible
+    nc = A.forward(q, k, v, 1.0, False)       # non-causal: row 0 scores 3, 0, 4; row 1 scores 0, -4, 3
+    assert nc["rmin"][0, 0, 0] == 0.0 and nc["rmin"][0, 0, 1] == -4.0
