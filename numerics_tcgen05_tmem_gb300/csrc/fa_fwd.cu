@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1) + ((uint32_t)lane_base << 16);
     const float c = p.scale_log2;
     float rm = -INFINITY, m = -INFINITY, l = 0.f;
+    float lc = 0.f;         // compensation of l: the row sum is l - lc (Kahan)
     float rmin = INFINITY;  // smallest visible raw score (statistics only)
     int rs = 0, ones = 0;
     int branch = 0;
@@ -382,7 +383,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kBlockN / 2; ++i)
           ones += ((pk[i] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((pk[i] >> 16) == 0x3F80u ? 1 : 0);
       }
-      l = fmaf(alpha, l, sum0 + sum1);
+      {
+        // l <- alpha l + rowsum(P~) with compensated (Kahan) summation across blocks; the
+        // rounding error of alpha * l is captured exactly by an FMA and folded in too
+        const float bsum = sum0 + sum1;
+        const float ls = alpha * l;
+        const float e = fmaf(alpha, l, -ls);
+        const float y = bsum - (alpha * lc - e);
+        const float tsum = ls + y;
+        lc = (tsum - ls) - y;
+        l = tsum;
+      }
       __syncwarp();
       {
         uint32_t w[32];
@@ -400,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // ------------------------------------------------------------ row results
     if (ok && nb > 0) {
+      l -= lc;  // fold the compensation in
       sh.lfin[t][r] = l;
       mbar_arrive(&sh.l_ready[t]);
       const float lse_row = m * p.scale + logf(l);
