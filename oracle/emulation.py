@@ -34,6 +34,9 @@ Readings where the pages are silent:
     block width.
   * l accumulates the FP32 P~ (before the BF16 cast): the softmax stays in
     FP32 and only the product with V is cast.
+  * FP8 forward (same page, §6.1: the shift carries over to FP8 with dynamic
+    scaling): P~ is multiplied by 2^8 and rounded to E4M3 (nearest, ties to
+    even) for the P~V product; l still sums the FP32 P~.
   * exp is evaluated in FP64 and rounded to FP32 (the GPU's exp is not
     reproduced bit for bit; results are compared within tolerances, and the
     exact-1.0 counts only where the margin to the BF16 rounding boundary is
@@ -49,6 +52,7 @@ from __future__ import annotations
 import numpy as np
 
 from .attention import BRANCH_BETA, BRANCH_RM, BRANCH_ZERO, _f64, visible
+from .fp8 import P_SCALE_LOG2, decode_e4m3, encode_e4m3
 
 BF16_ONE_BITS = 0x3F80
 
@@ -82,17 +86,23 @@ def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: 
     """Blocked online-softmax forward over key blocks of width ``block_n``.
 
     precision="bf16": FP32 state, P~ rounded to BF16 for P~V, O rounded to BF16.
+    precision="fp8": the same, but P~ * 2^8 is rounded to E4M3 for P~V (the FP8
+    forward; pass the dequantised Q, K, V).
     precision="fp64": the same recurrence with every value in FP64 and no
     rounding (used to pin the recurrence against the one-shot definition).
 
     Returns dict(o, lse, rm, rs, branch, m, ones) per [B, H, N]; ``ones`` is
-    the number of visible P~ entries of a row whose BF16 value is exactly 1.0
-    (counted per block, as the blocks are processed).
+    the number of visible P~ entries of a row whose rounded value (BF16, or
+    E4M3 of P~ * 2^8 divided by 2^8) is exactly 1.0 (counted per block, as the
+    blocks are processed).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, N, d = q.shape
     dv = v.shape[-1]
-    ft = np.float32 if precision == "bf16" else np.float64
+    if precision not in ("bf16", "fp8", "fp64"):
+        raise ValueError(precision)
+    low = precision != "fp64"
+    ft = np.float32 if low else np.float64
     beta_t = ft(beta)
     res = {key: np.zeros((B, H, N), dtype=ft) for key in ("lse", "rm", "m")}
     res["o"] = np.zeros((B, H, N, dv), dtype=ft)
@@ -137,8 +147,12 @@ def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: 
                                np.exp(scale * (s.astype(np.float64) - np.where(live, m_new, 0.0)[:, None].astype(np.float64))),
                                0.0)
                 p = e64.astype(ft)
-                if precision == "bf16":
-                    pb = round_bf16(p)
+                if low:
+                    if precision == "bf16":
+                        pb = round_bf16(p)
+                    else:
+                        ps = np.float32(2.0 ** P_SCALE_LOG2)
+                        pb = (decode_e4m3(encode_e4m3((p * ps).astype(np.float32))) / float(ps)).astype(np.float32)
                     ones += ((pb == np.float32(1.0)) & vis).sum(axis=1)
                     rowsum = p.sum(axis=1, dtype=np.float32)
                     l = (alpha * l).astype(ft) + rowsum
@@ -150,7 +164,7 @@ def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: 
                     acc = alpha[:, None] * acc + p @ v[b, h, cols]
                 m = m_new
             o = acc / l[:, None]
-            if precision == "bf16":
+            if low:
                 o = round_bf16(o.astype(np.float32))
                 lse = (ft(scale) * m).astype(ft) + np.log(l.astype(np.float64)).astype(ft)
             else:
