@@ -10,7 +10,8 @@
  *            final O = diag(l)^-1 O; §3.1 delta = rowsum(dO o O) in the
  *            backward; §4.1/§4.2 the stabilised safe softmax (a repeated row
  *            maximum moves the shift to beta*rm for rm > 0 or to 0 for rm < 0;
- *            beta in [1.1, 1.5], 1.25 recommended); §7.1 the monitor
+ *            beta in [1.1, 1.5], 1.25 recommended); §6.1 the fix carries over
+ *            to FP8 with dynamic scaling factors; §7.1 the monitor
  *            (S == rowmax(S)).sum().
  *   [jsqmd]  "Flash Attention低精度训练稳定性优化实践" §3.2: QK^T accumulated in
  *            FP32, softmax in FP32, the product with V in BF16; §3.3 the
@@ -98,6 +99,39 @@ typedef struct {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            int causal, float scale, int stable, float beta, const fa_row_stats* stats, void* stream);
+
+/*
+ * fa_quantize_fp8 -- dynamic per-tensor FP8 scaling ([ijyty §6.1]: the stabilised
+ * shift carries over to FP8 when paired with dynamic scaling factors; the page gives no
+ * formula, this is the usual amax rule).
+ *   x        : input, BF16, n elements (any shape, contiguous), device, 16-byte aligned
+ *   x8       : output, E4M3 codes (1 byte each), n elements, device, 16-byte aligned
+ *   descale  : output, one FP32 on the device: amax(|x|) / 448 (1 if x is all zero)
+ *   x8[i] = E4M3(x[i] / descale) -- FP32 division, round to nearest even, saturating at
+ *   +-448 -- so x is represented by x8 * descale.  Four launches on `stream`; descale is
+ *   used as the amax scratch until the last one.  NaN or Inf in x give a NaN or Inf descale.
+ * Returns FA_OK, FA_ERR_INVALID_ARG or FA_ERR_CUDA.
+ */
+int fa_quantize_fp8(const void* x, size_t n, void* x8, float* descale, void* stream);
+
+/*
+ * fa_fwd_fp8 -- the forward of fa_fwd with E4M3 inputs ([ijyty §6.1], FP8 with dynamic
+ * scaling).  Q K^T and P~ V run as E4M3 x E4M3 tensor-core products with FP32
+ * accumulation; the softmax runs in FP32 as in fa_fwd.
+ *   q8, k8, v8 : E4M3 codes, [B,H,N,d] contiguous, device, 16-byte aligned
+ *   descale    : device FP32[3] = the per-tensor scales of Q, K, V (fa_quantize_fp8's
+ *                outputs); the inputs are q8 * descale[0], k8 * descale[1], v8 * descale[2]
+ *   o, lse     : as fa_fwd (O in BF16, lse of the dequantised scores)
+ *   the raw scores, the row maximum, the tie count and the shift rule are those of the
+ *   dequantised scores (q8 dq).(k8 dk); P~ is multiplied by 2^8 and rounded to E4M3 for the
+ *   P~V product; stats->row_max_raw / row_min_raw are in dequantised units and
+ *   stats->row_ones counts P~ entries whose E4M3 value is exactly 1.0 (2^8 after scaling).
+ *   d must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA.
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale, void* o, float* lse,
+               int B, int H, int N, int d, int causal, float scale, int stable, float beta,
+               const fa_row_stats* stats, void* stream);
 
 /*
  * fa_bwd_workspace_size -- bytes of device scratch fa_bwd needs: an FP32

@@ -24,8 +24,8 @@ FA_ERR_DEVICE_BOUNDS = 5
 FA_WARN_NONFINITE = 6
 
 # every symbol include/fa.h declares
-EXPORTS = ("fa_fwd", "fa_bwd", "fa_bwd_staged", "fa_bwd_noalloc", "fa_bwd_workspace_size", "fa_device_status",
-           "fa_last_error", "fa_version")
+EXPORTS = ("fa_fwd", "fa_fwd_fp8", "fa_quantize_fp8", "fa_bwd", "fa_bwd_staged", "fa_bwd_noalloc",
+           "fa_bwd_workspace_size", "fa_device_status", "fa_last_error", "fa_version")
 
 # size of the fixed device scratch behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in fa.h)
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -59,6 +59,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     vp, ci, cf, cs = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, ctypes.POINTER(RowStats), vp]
     L.fa_fwd.restype = ci
+    L.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, cf, ctypes.POINTER(RowStats), vp]
+    L.fa_fwd_fp8.restype = ci
+    L.fa_quantize_fp8.argtypes = [vp, cs, vp, vp, vp]
+    L.fa_quantize_fp8.restype = ci
     L.fa_bwd_workspace_size.argtypes = [ci, ci, ci, ci]
     L.fa_bwd_workspace_size.restype = cs
     L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, vp, cs, vp]
@@ -108,13 +112,30 @@ def _check_qkv(*ts):
 
 def fa_fwd(q, k, v, o, lse, causal: bool, scale: float, stable: int, beta: float, stats=None, stream=None) -> int:
     B, H, N, d = q.shape
-    st = None
-    if stats is not None:
-        st = RowStats(*(None if stats.get(n) is None else stats[n].data_ptr()
-                        for n in ("row_max_raw", "row_ties", "row_branch", "row_ones", "row_min_raw")))
+    st = _row_stats(stats)
     return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, int(bool(causal)),
                          float(scale), int(stable), float(beta), ctypes.byref(st) if st is not None else None,
                          _stream(stream))
+
+
+def _row_stats(stats):
+    if stats is None:
+        return None
+    return RowStats(*(None if stats.get(n) is None else stats[n].data_ptr()
+                      for n in ("row_max_raw", "row_ties", "row_branch", "row_ones", "row_min_raw")))
+
+
+def fa_fwd_fp8(q8, k8, v8, descale, o, lse, causal: bool, scale: float, stable: int, beta: float, stats=None,
+               stream=None) -> int:
+    B, H, N, d = q8.shape
+    st = _row_stats(stats)
+    return load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(descale), _ptr(o), _ptr(lse), B, H, N, d,
+                             int(bool(causal)), float(scale), int(stable), float(beta),
+                             ctypes.byref(st) if st is not None else None, _stream(stream))
+
+
+def fa_quantize_fp8(x, x8, descale, stream=None) -> int:
+    return load().fa_quantize_fp8(_ptr(x), int(x.numel()), _ptr(x8), _ptr(descale), _stream(stream))
 
 
 def fa_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
@@ -146,6 +167,14 @@ def fa_device_status(stream=None) -> int:
 
 # ----------------------------------------------------------------- tensor-level helpers
 
+def _stats_dict(B, H, N, device):
+    return {"row_max_raw": torch.empty((B, H, N), device=device, dtype=torch.float32),
+            "row_ties": torch.empty((B, H, N), device=device, dtype=torch.int32),
+            "row_branch": torch.empty((B, H, N), device=device, dtype=torch.int8),
+            "row_ones": torch.empty((B, H, N), device=device, dtype=torch.int32),
+            "row_min_raw": torch.empty((B, H, N), device=device, dtype=torch.float32)}
+
+
 def forward(q, k, v, causal: bool = True, scale=None, stable: int = 1, beta: float = 1.25, stats: bool = False,
             stream=None):
     """Returns (o, lse) or (o, lse, stats_dict); outputs are freshly allocated."""
@@ -154,14 +183,40 @@ def forward(q, k, v, causal: bool = True, scale=None, stable: int = 1, beta: flo
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
-    sd = None
-    if stats:
-        sd = {"row_max_raw": torch.empty((B, H, N), device=q.device, dtype=torch.float32),
-              "row_ties": torch.empty((B, H, N), device=q.device, dtype=torch.int32),
-              "row_branch": torch.empty((B, H, N), device=q.device, dtype=torch.int8),
-              "row_ones": torch.empty((B, H, N), device=q.device, dtype=torch.int32),
-              "row_min_raw": torch.empty((B, H, N), device=q.device, dtype=torch.float32)}
+    sd = _stats_dict(B, H, N, q.device) if stats else None
     _check(fa_fwd(q, k, v, o, lse, causal, scale, stable, beta, sd, stream))
+    return (o, lse, sd) if stats else (o, lse)
+
+
+def quantize_fp8(x, stream=None):
+    """Dynamic per-tensor E4M3 scaling of a contiguous CUDA bfloat16 tensor.
+
+    Returns (x8, descale): x8 holds the E4M3 codes as uint8 with x's shape, descale is a
+    1-element FP32 CUDA tensor; x is represented by x8 * descale.
+    """
+    if not (x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()):
+        raise ValueError("expected a contiguous CUDA bfloat16 tensor")
+    x8 = torch.empty(x.shape, device=x.device, dtype=torch.uint8)
+    descale = torch.empty(1, device=x.device, dtype=torch.float32)
+    _check(fa_quantize_fp8(x, x8, descale, stream))
+    return x8, descale
+
+
+def forward_fp8(q8, k8, v8, descale, causal: bool = True, scale=None, stable: int = 1, beta: float = 1.25,
+                stats: bool = False, stream=None):
+    """FP8 forward: q8, k8, v8 are uint8 E4M3 codes [B, H, N, d]; descale is an FP32 CUDA
+    tensor of 3 per-tensor scales (Q, K, V).  Returns (o, lse) or (o, lse, stats_dict)."""
+    for t in (q8, k8, v8):
+        if not (t.is_cuda and t.dtype == torch.uint8 and t.is_contiguous() and t.dim() == 4 and t.shape == q8.shape):
+            raise ValueError("expected contiguous CUDA uint8 tensors of one shape [B, H, N, d]")
+    if not (descale.is_cuda and descale.dtype == torch.float32 and descale.numel() == 3 and descale.is_contiguous()):
+        raise ValueError("descale must be a contiguous CUDA float32 tensor of 3 elements")
+    B, H, N, d = q8.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = torch.empty((B, H, N, d), device=q8.device, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, N), device=q8.device, dtype=torch.float32)
+    sd = _stats_dict(B, H, N, q8.device) if stats else None
+    _check(fa_fwd_fp8(q8, k8, v8, descale, o, lse, causal, scale, stable, beta, sd, stream))
     return (o, lse, sd) if stats else (o, lse)
 
 

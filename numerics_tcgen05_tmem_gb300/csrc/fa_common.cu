@@ -92,6 +92,10 @@ int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int
   return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, BH, N, d, 64, box_rows);
 }
 
+int make_tmap_u8_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, BH, N, d, 128, box_rows);
+}
+
 int make_tmap_f32_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
   return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, BH, N, d, 32, box_rows);
 }

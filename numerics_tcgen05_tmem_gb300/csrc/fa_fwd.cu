@@ -42,6 +42,7 @@ constexpr int kTiles = 2;      // query tiles per CTA
 constexpr int kThreads = 512;  // 16 warps
 constexpr int kMmaWarp = 12;
 constexpr int kLoadWarp = 13;  // warps 14-15 only take part in set-up and teardown
+constexpr int kPScaleLog2 = 8;  // FP8 path: P~ is scaled by 2^8 before its E4M3 rounding
 // Per-thread register budgets after the launch (setmaxnreg); the launch gives every thread
 // kRegLaunch registers and the split below must not exceed 512 * kRegLaunch.
 constexpr int kRegLaunch = 128;
@@ -49,17 +50,28 @@ constexpr int kRegSoftmax = 176, kRegCorr = 96, kRegOther = 56;
 static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther <= kThreads * kRegLaunch,
               "register split exceeds the launch allocation");
 
-template <int D>
+// kFp8: Q, K, V (and P~ for the P~V product) are E4M3 instead of BF16.  Every operand row
+// is then D bytes, so a 128-byte swizzle atom spans 128 elements instead of 64, and one MMA
+// instruction consumes 32 elements of K instead of 16 -- always 32 bytes per k-step.
+template <int D, bool kFp8 = false>
 struct Cfg {
-  static constexpr int kStages = (D == 128) ? 2 : 4;
-  static constexpr int kTileBytes = kBlockM * D * 2;   // one 128 x D BF16 tile (Q, K or V)
+  static constexpr int kElem = kFp8 ? 1 : 2;                // bytes per Q/K/V element
+  static constexpr int kStages = kFp8 ? 4 : ((D == 128) ? 2 : 4);
+  static constexpr int kTileBytes = kBlockM * D * kElem;    // one 128 x D tile (Q, K or V)
+  static constexpr int kAtoms = D * kElem / 128;            // 128-byte column blocks of a tile
+  static constexpr int kAtomElems = 128 / kElem;            // elements per 128-byte row of an atom
+  static constexpr int kKStepsS = D * kElem / 32;           // Q K^T k-steps (32 bytes each)
+  static constexpr int kKStepsO = kBlockN * kElem / 32;     // P~ V k-steps over the keys
+  static constexpr int kPCols = kBlockN * kElem / 4;        // TMEM columns of a packed P~ row
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kVOff + kStages * kTileBytes + 1024;  // +1024 for alignment
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + D;
-  static constexpr uint32_t kIdescS = idesc_bf16(128, kBlockN, false, false);  // Q K^T, both K-major
-  static constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);         // P~ (TMEM) x V (MN-major)
+  // Q K^T with both operands K-major; P~ (TMEM) x V with V MN-major
+  static constexpr uint32_t kIdescS = kFp8 ? idesc_e4m3(128, kBlockN, false, false) : idesc_bf16(128, kBlockN, false, false);
+  static constexpr uint32_t kIdescO = kFp8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
+  static_assert(kAtoms >= 1, "a tile row must fill at least one 128-byte swizzle atom");
 };
 
 struct Params {
@@ -77,6 +89,7 @@ struct Params {
   int causal;
   float scale;
   float scale_log2;  // scale * log2(e)
+  const float* descale;  // FP8 inputs: device [3] = per-tensor scales of Q, K, V
   float beta;
   int inject_stall;  // test builds only (FA_TEST_HOOKS): make the MMA warp's first wait run out
 };
@@ -108,11 +121,11 @@ __device__ __forceinline__ int tile_blocks(const Params& p, int qb, int t) {
 // kStable: 0 = plain shift (running max); 1 = stabilised shift on the running (max, count)
 // of the row; 2 = block-local reading: each key block's own (max, count) picks a shift by
 // the same rule and the row keeps the largest shift seen so far.
-template <int D, int kStable, bool kStats>
+template <int D, int kStable, bool kStats, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kFp8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Shared sh;
@@ -167,8 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ntiles = (nb1 > 0) ? 2 : 1;
       mbar_arrive_expect_tx(&sh.q_full, ntiles * C::kTileBytes);
       for (int t = 0; t < ntiles; ++t)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * 16384, &tmQ, &sh.q_full, c * 64,
+        for (int c = 0; c < C::kAtoms; ++c)
+          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * 16384, &tmQ, &sh.q_full, c * C::kAtomElems,
                       qb * (kTiles * kBlockM) + t * kBlockM, bh);
       int nk_issued = 0, nv_issued = 0;
       for (int j = 0; j < nbmax; ++j) {
@@ -176,13 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (j / C::kStages) & 1;
         if (!mbar_wait(&sh.k_empty[s], ph ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&sh.k_full[s], C::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * 16384, &tmK, &sh.k_full[s], c * 64, j * kBlockN, bh);
+        for (int c = 0; c < C::kAtoms; ++c)
+          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * 16384, &tmK, &sh.k_full[s], c * C::kAtomElems,
+                      j * kBlockN, bh);
         nk_issued = j + 1;
         if (!mbar_wait(&sh.v_empty[s], ph ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&sh.v_full[s], C::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + c * 16384, &tmV, &sh.v_full[s], c * 64, j * kBlockN, bh);
+        for (int c = 0; c < C::kAtoms; ++c)
+          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + c * 16384, &tmV, &sh.v_full[s], c * C::kAtomElems,
+                      j * kBlockN, bh);
         nv_issued = j + 1;
       }
       if (*abort_flag) {
@@ -214,20 +229,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a0 = sQ + t * C::kTileBytes, b0 = sK + s * C::kTileBytes;
         const uint32_t d = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::kKStepsS; ++kk) {
           const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::kIdescS, kk > 0);
+          if constexpr (kFp8)
+            mma_ss_f8(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::kIdescS, kk > 0);
+          else
+            mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::kIdescS, kk > 0);
         }
         tc_commit(&sh.s_full[t]);
       };
-      // O_t += P~_t V_j: P~ from TMEM (K = 128 keys, 8 columns per k-step), V MN-major
+      // O_t += P~_t V_j: P~ from TMEM (K = 128 keys, 8 columns = 32 bytes per k-step), V MN-major
+      // (a k-step covers 32 / kElem keys of 128-byte rows)
       auto issue_pv = [&](int t, int s, int j) {
         const uint32_t b0 = sV + s * C::kTileBytes;
         const uint32_t d = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1);
         const uint32_t a = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          mma_ts(d, a + kk * 8, sdesc_sw128(b0 + kk * 2048, 16384, 1024), C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::kKStepsO; ++kk) {
+          const uint64_t bd = sdesc_sw128(b0 + kk * (32 / C::kElem) * 128, 16384, 1024);
+          if constexpr (kFp8)
+            mma_ts_f8(d, a + kk * 8, bd, C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+          else
+            mma_ts(d, a + kk * 8, bd, C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
         tc_commit(&sh.pv_done[t]);
       };
       // Order: S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 PV1_1 S1_2 | ... | PV0_last PV1_last
@@ -275,7 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nb = (t == 0) ? nb0 : nb1;
     const int row = qb * (kTiles * kBlockM) + t * kBlockM + r;
     const uint32_t tS = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1) + ((uint32_t)lane_base << 16);
-    const float c = p.scale_log2;
+    // FP8: raw scores are in units of dq * dk (the Q and K scales); fold both into the
+    // exponent's scale.  rm, m and the tie count stay in accumulator units, which is the same
+    // rule on the dequantised scores (a positive factor keeps order, equality and sign).
+    float dqk = 1.f;
+    if constexpr (kFp8) dqk = __ldg(p.descale) * __ldg(p.descale + 1);
+    const float c = p.scale_log2 * dqk;
     float rm = -INFINITY, m = -INFINITY, l = 0.f;
     float lc = 0.f;         // compensation of l: the row sum is l - lc (Kahan)
     float rmin = INFINITY;  // smallest visible raw score (statistics only)
@@ -366,22 +395,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         sh.alpha[t][r] = alpha;
         mbar_arrive(&sh.alpha_ready[t]);
       }
-      const float nmc = -m_new * c;
-      uint32_t pk[kBlockN / 2];
+      // FP8: P~ * 2^8 (added to the exponent) uses the E4M3 range below 448 instead of <= 1
+      const float nmc = kFp8 ? fmaf(-m_new, c, (float)kPScaleLog2) : -m_new * c;
       float sum0 = 0.f, sum1 = 0.f;
+      if constexpr (kFp8) {
+        uint32_t pk[kBlockN / 4];
 #pragma unroll
-      for (int i = 0; i < kBlockN; i += 2) {
-        float x0, x1;
-        fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);   // scale*log2(e) * (S - m)
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        add2(sum0, sum1, sum0, sum1, p0, p1);
-        pk[i / 2] = pack_bf16x2(p0, p1);
-      }
-      if constexpr (kStats) {
+        for (int i = 0; i < kBlockN; i += 4) {
+          float x0, x1, x2, x3;
+          fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);       // scale*log2(e)*dq*dk * (S - m) + 8
+          fma2(x2, x3, sv[i + 2], sv[i + 3], c, c, nmc, nmc);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          add2(sum0, sum1, sum0, sum1, p0, p1);
+          add2(sum0, sum1, sum0, sum1, p2, p3);
+          pk[i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+        }
+        if constexpr (kStats) {
+          // an entry of exactly 1.0 is 2^8 = E4M3 code 0x78 after the scaling
 #pragma unroll
-        for (int i = 0; i < kBlockN / 2; ++i)
-          ones += ((pk[i] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((pk[i] >> 16) == 0x3F80u ? 1 : 0);
+          for (int i = 0; i < kBlockN / 4; ++i)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) ones += (((pk[i] >> (8 * b)) & 0xFFu) == 0x78u) ? 1 : 0;
+        }
+        __syncwarp();
+        tmem_st32(tS, pk);
+      } else {
+        uint32_t pk[kBlockN / 2];
+#pragma unroll
+        for (int i = 0; i < kBlockN; i += 2) {
+          float x0, x1;
+          fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);   // scale*log2(e) * (S - m)
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          add2(sum0, sum1, sum0, sum1, p0, p1);
+          pk[i / 2] = pack_bf16x2(p0, p1);
+        }
+        if constexpr (kStats) {
+#pragma unroll
+          for (int i = 0; i < kBlockN / 2; ++i)
+            ones += ((pk[i] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((pk[i] >> 16) == 0x3F80u ? 1 : 0);
+        }
+        __syncwarp();
+        uint32_t w[32];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = pk[h * 32 + i];
+          tmem_st32(tS + h * 32, w);
+        }
       }
       {
         // l <- alpha l + rowsum(P~) with compensated (Kahan) summation across blocks; the
@@ -394,16 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         lc = (tsum - ls) - y;
         l = tsum;
       }
-      __syncwarp();
-      {
-        uint32_t w[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = pk[h * 32 + i];
-          tmem_st32(tS + h * 32, w);
-        }
-      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sh.p_ready[t]);
@@ -414,17 +465,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       l -= lc;  // fold the compensation in
       sh.lfin[t][r] = l;
       mbar_arrive(&sh.l_ready[t]);
-      const float lse_row = m * p.scale + logf(l);
+      // FP8: l sums P~ * 2^8
+      const float lse_row = kFp8 ? m * (p.scale * dqk) + (logf(l) - (float)kPScaleLog2 * 0.6931471805599453f)
+                                 : m * p.scale + logf(l);
       report_nonfinite(row < p.N && !(fabsf(lse_row) < INFINITY), p.status);
       if (row < p.N) {
         const size_t srow = (size_t)bh * p.N + row;
         p.lse[srow] = lse_row;
         if constexpr (kStats) {
-          if (p.stat_rm) p.stat_rm[srow] = rm;
+          if (p.stat_rm) p.stat_rm[srow] = rm * dqk;
           if (p.stat_rs) p.stat_rs[srow] = rs;
           if (p.stat_branch) p.stat_branch[srow] = (int8_t)branch;
           if (p.stat_ones) p.stat_ones[srow] = ones;
-          if (p.stat_min) p.stat_min[srow] = rmin;
+          if (p.stat_min) p.stat_min[srow] = rmin * dqk;
         }
       }
     }
@@ -474,7 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(&sh.pv_done[t], (nb[t] - 1) & 1, abort_flag, p.status))) break;
       if (!(ok = mbar_wait(&sh.l_ready[t], 0, abort_flag, p.status))) break;
       tc_fence_after();
-      const float inv_l = 1.f / sh.lfin[t][r];
+      // FP8: O = (P~ 2^8)_E4M3 V8 * dv / (l 2^8); the 2^8 is in both sums
+      const float inv_l = (kFp8 ? __ldg(p.descale + 2) : 1.f) / sh.lfin[t][r];
       const int row = qb * (kTiles * kBlockM) + t * kBlockM + r;
       const bool valid = row < p.N;
       const size_t orow = ((size_t)bh * p.N + (valid ? row : 0)) * D;
@@ -518,11 +572,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <int D, int kStable, bool kStats>
+template <int D, int kStable, bool kStats, bool kFp8>
 int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::fwd::Params& p,
                cudaStream_t stream) {
-  using C = fa::fwd::Cfg<D>;
-  auto kern = fa::fwd::fa_fwd_kernel<D, kStable, kStats>;
+  using C = fa::fwd::Cfg<D, kFp8>;
+  auto kern = fa::fwd::fa_fwd_kernel<D, kStable, kStats, kFp8>;
   int rc = fa::check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                           "cudaFuncSetAttribute(fwd)");
   if (rc) return rc;
@@ -539,20 +593,21 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   return fa::check_cuda(cudaGetLastError(), "launch fa_fwd_kernel");
 }
 
-template <int D>
+template <int D, bool kFp8>
 int dispatch_fwd(int stable, bool stats, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const fa::fwd::Params& p, cudaStream_t s) {
-  if (stable == 2) return stats ? launch_fwd<D, 2, true>(tq, tk, tv, p, s) : launch_fwd<D, 2, false>(tq, tk, tv, p, s);
-  if (stable == 1) return stats ? launch_fwd<D, 1, true>(tq, tk, tv, p, s) : launch_fwd<D, 1, false>(tq, tk, tv, p, s);
-  return stats ? launch_fwd<D, 0, true>(tq, tk, tv, p, s) : launch_fwd<D, 0, false>(tq, tk, tv, p, s);
+  if (stable == 2)
+    return stats ? launch_fwd<D, 2, true, kFp8>(tq, tk, tv, p, s) : launch_fwd<D, 2, false, kFp8>(tq, tk, tv, p, s);
+  if (stable == 1)
+    return stats ? launch_fwd<D, 1, true, kFp8>(tq, tk, tv, p, s) : launch_fwd<D, 1, false, kFp8>(tq, tk, tv, p, s);
+  return stats ? launch_fwd<D, 0, true, kFp8>(tq, tk, tv, p, s) : launch_fwd<D, 0, false, kFp8>(tq, tk, tv, p, s);
 }
 
-}  // namespace
-
-extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-                      int causal, float scale, int stable, float beta, const fa_row_stats* stats, void* stream) {
+// Argument checks and kernel parameters shared by the BF16 and FP8 entry points.
+int prepare_fwd(fa::fwd::Params& p, bool& want_stats, const void* q, const void* k, const void* v, void* o,
+                float* lse, int B, int H, int N, int d, int causal, float scale, int stable, float beta,
+                const fa_row_stats* stats) {
   using namespace fa;
-  clear_error();
   int rc;
   if ((rc = check_shape(B, H, N, d))) return rc;
   if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) || (rc = check_ptr(o, "o")))
@@ -561,10 +616,10 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   if (!(scale > 0.f) || !isfinite(scale)) return set_error(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (stable < 0 || stable > 2) return set_error(FA_ERR_INVALID_ARG, "stable must be 0, 1 or 2 (got %d)", stable);
   if (stable && (!isfinite(beta) || beta < 1.f)) return set_error(FA_ERR_INVALID_ARG, "beta must be finite and >= 1");
-  fwd::Params p{};
+  p = fwd::Params{};
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
-  bool want_stats = false;
+  want_stats = false;
   if (stats) {
     p.stat_rm = stats->row_max_raw;
     p.stat_rs = stats->row_ties;
@@ -586,11 +641,45 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   const char* inject = getenv("FA_TEST_INJECT_STALL");
   p.inject_stall = (inject && inject[0] == '1') ? 1 : 0;
 #endif
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                      int causal, float scale, int stable, float beta, const fa_row_stats* stats, void* stream) {
+  using namespace fa;
+  clear_error();
+  fwd::Params p;
+  bool want_stats;
+  int rc = prepare_fwd(p, want_stats, q, k, v, o, lse, B, H, N, d, causal, scale, stable, beta, stats);
+  if (rc) return rc;
   CUtensorMap tq, tk, tv;
   if ((rc = make_tmap_bhnd(&tq, q, B * H, N, d, fwd::kBlockM)) || (rc = make_tmap_bhnd(&tk, k, B * H, N, d, fwd::kBlockN)) ||
       (rc = make_tmap_bhnd(&tv, v, B * H, N, d, fwd::kBlockN)))
     return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return d == 64 ? dispatch_fwd<64>(stable, want_stats, tq, tk, tv, p, s)
-                 : dispatch_fwd<128>(stable, want_stats, tq, tk, tv, p, s);
+  return d == 64 ? dispatch_fwd<64, false>(stable, want_stats, tq, tk, tv, p, s)
+                 : dispatch_fwd<128, false>(stable, want_stats, tq, tk, tv, p, s);
+}
+
+extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale, void* o, float* lse,
+                          int B, int H, int N, int d, int causal, float scale, int stable, float beta,
+                          const fa_row_stats* stats, void* stream) {
+  using namespace fa;
+  clear_error();
+  if (d != 128) return set_error(FA_ERR_UNSUPPORTED, "the FP8 forward supports d=128 only (got %d)", d);
+  if (!descale) return set_error(FA_ERR_INVALID_ARG, "descale is NULL");
+  if (reinterpret_cast<uintptr_t>(descale) & 3) return set_error(FA_ERR_INVALID_ARG, "descale is not 4-byte aligned");
+  fwd::Params p;
+  bool want_stats;
+  int rc = prepare_fwd(p, want_stats, q8, k8, v8, o, lse, B, H, N, d, causal, scale, stable, beta, stats);
+  if (rc) return rc;
+  p.descale = descale;
+  CUtensorMap tq, tk, tv;
+  if ((rc = make_tmap_u8_bhnd(&tq, q8, B * H, N, d, fwd::kBlockM)) ||
+      (rc = make_tmap_u8_bhnd(&tk, k8, B * H, N, d, fwd::kBlockN)) ||
+      (rc = make_tmap_u8_bhnd(&tv, v8, B * H, N, d, fwd::kBlockN)))
+    return rc;
+  return dispatch_fwd<128, true>(stable, want_stats, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
 }

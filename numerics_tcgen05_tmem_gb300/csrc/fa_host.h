@@ -25,6 +25,10 @@ uint32_t* device_status_word();
 // 128-byte swizzle and a (64 x box_rows x 1) box; out-of-range rows read as zero.
 int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
 
+// The same for a 1-byte (E4M3) tensor: a (128 x box_rows x 1) box, one 128-byte row per
+// box row when d = 128.
+int make_tmap_u8_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
+
 // Encode a 3-D FP32 tensor map over a contiguous [BH, N, d] tensor with a 128-byte swizzle
 // and a (32 x box_rows x 1) box (for TMA reductions into an FP32 accumulator).
 int make_tmap_f32_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);

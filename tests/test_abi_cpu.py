@@ -82,3 +82,23 @@ def test_backward_invalid_arguments(lib):
                     good, ws - 256, None)
     assert rc == binding.FA_ERR_INVALID_ARG
     assert b"workspace" in lib.fa_last_error()
+
+
+def test_fp8_invalid_arguments(lib):
+    good = ctypes.c_void_p(1 << 20)
+    ds = ctypes.c_void_p(1 << 21)
+
+    def fwd8(q=good, descale=ds, d=128, N=128, stable=1):
+        return lib.fa_fwd_fp8(q, good, good, descale, good, good, 1, 1, N, d, 1, 0.125, stable, 1.25, None, None)
+
+    assert fwd8(d=64) == binding.FA_ERR_UNSUPPORTED
+    assert b"d=128" in lib.fa_last_error()
+    assert fwd8(descale=None) == binding.FA_ERR_INVALID_ARG
+    assert fwd8(descale=ctypes.c_void_p((1 << 21) + 2)) == binding.FA_ERR_INVALID_ARG
+    assert fwd8(q=None) == binding.FA_ERR_INVALID_ARG
+    assert fwd8(N=0) == binding.FA_ERR_INVALID_ARG
+    assert fwd8(stable=5) == binding.FA_ERR_INVALID_ARG
+    assert lib.fa_quantize_fp8(None, 16, good, ds, None) == binding.FA_ERR_INVALID_ARG
+    assert lib.fa_quantize_fp8(good, 16, ctypes.c_void_p((1 << 20) + 4), ds, None) == binding.FA_ERR_INVALID_ARG
+    assert lib.fa_quantize_fp8(good, 16, good, None, None) == binding.FA_ERR_INVALID_ARG
+    assert b"descale" in lib.fa_last_error()

@@ -98,6 +98,19 @@ def test_no_stats_pointer_path_matches():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_nan_key_reaches_every_output_row():
+    # a NaN key column poisons every row's scores: the shift ignores it (max skips NaN) but
+    # its exponential is NaN, so every row of O and the LSE turn NaN and the call reports it
+    w = inputs.random_case(1, 1, 512, 64, False, seed=8)
+    q, k, v, _ = to_dev(w)
+    k[0, 0, 130, 0] = float("nan")
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)
+    assert binding.fa_fwd(q, k, v, o, lse, False, w.scale, 1, 1.25) == binding.FA_OK
+    assert binding.fa_device_status() == binding.FA_WARN_NONFINITE
+    assert torch.isnan(o.float()).all() and torch.isnan(lse).all()
+
+
 def test_llama7b_full_size_sampled_heads():
     # full 8192-token, 32-head problem on the GPU; the oracle checks two heads
     w = inputs.llama7b_long()
