@@ -162,6 +162,8 @@ def kernel_sources_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "numerics_tcgen05_tmem_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
+        if not f.endswith((".cu", ".cuh", ".h")):
+            continue
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -388,6 +390,7 @@ def run_native(args):
             "kernel": "fa_fwd_kernel<128,stable,fp8>", "tflops": round(ff / (fp8_ms * 1e-3) / 1e12, 1),
             "ms": round(fp8_ms, 4), "launches_timed": R8,
             "peak": round(2 * peak, 1), "frac": round(ff / (fp8_ms * 1e-3) / 1e12 / (2 * peak), 4),
+            "traffic": profiled_traffic("fwd_fp8"),
             "peak_source": "measured dense BF16 burst x 2 (nominal FP8/BF16 dense ratio 4.5/2.25)",
             "quantize_ms_per_tensor": round(quant_ms, 4),
             "quantize_gbs": round(5 * q.numel() / (quant_ms * 1e-3) / 1e9, 1),
