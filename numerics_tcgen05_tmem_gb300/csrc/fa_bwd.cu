@@ -14,17 +14,18 @@
 //   fa_bwd_main:       one CTA per (b, h, 128-key tile); loops over query tiles
 //   fa_bwd_dq_convert: dq = bf16(scale * dQ_acc)
 //
-// fa_bwd_main CTA organisation (448 threads):
+// fa_bwd_main CTA organisation (512 threads, registers rebalanced per warpgroup):
 //   warps 0-7  two "softmax" warpgroups; thread = key row (TMEM lane) of the tile,
 //              warpgroup h takes query columns [64h, 64h+64):
 //              P^T = exp2(S^T c - lse_q log2 e) into TMEM (BF16) for the dV MMA,
 //              dS^T = P^T o (dP^T - delta_q) as BF16 into its dP^T columns of TMEM (the A
 //              operand of the dK MMA) and into shared memory (128B swizzle; the MN-major
 //              A operand of the dQ MMA); finally warpgroup 0 writes dK, 1 writes dV.
-//   warps 8-11 dQ warpgroup: thread = query row; loads each dQ tile from TMEM, hands
-//              the columns back, then reduces it into the FP32 dQ accumulator.
+//   warps 8-11 dQ warpgroup: thread = query row; loads each dQ tile from TMEM in one
+//              round trip, hands the columns back, then reduces it into the FP32 dQ
+//              accumulator through shared-memory staging and TMA reduce-adds.
 //   warp  12   MMA issuer;  warp 13  TMA producer (Q, dO tiles and the per-tile
-//              lse / delta vectors, double-buffered).
+//              lse / delta vectors, double-buffered);  warps 14-15 set-up/teardown only.
 // Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -38,9 +39,16 @@ namespace fa {
 namespace bwd {
 
 constexpr int kBlock = 128;     // keys per CTA tile and queries per step
-constexpr int kThreads = 448;   // 14 warps
+constexpr int kThreads = 512;   // 16 warps; warps 14-15 only take part in set-up and teardown
 constexpr int kMmaWarp = 12;
 constexpr int kLoadWarp = 13;
+// Per-thread register budgets after the launch (setmaxnreg): the dQ warpgroup holds a whole
+// dQ row (D FP32) so it can hand the TMEM columns back in one round trip, the P/dS
+// warpgroups hold a 64-column row of P and dP, the MMA/TMA warpgroup needs few.
+constexpr int kRegLaunch = 128;
+constexpr int kRegPdS = 144, kRegDQ = 152, kRegOther = 72;
+static_assert(2 * 128 * kRegPdS + 128 * kRegDQ + 128 * kRegOther <= kThreads * kRegLaunch,
+              "register split exceeds the launch allocation");
 constexpr int kStages = 2;      // Q-tile ring depth (dO is single-buffered)
 
 template <int D>
@@ -211,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
 
+  if (warp >= 12) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther));
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (elect_one()) {
@@ -343,8 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&sh.mma_done, 0, &ignore_abort, p.status);
       }
     }
+  }
   } else if (warp < 8) {
     // ------------------------------------------------------------------ P^T / dS^T warpgroups
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegPdS));
     // warpgroup h handles query columns [64h, 64h + 64) of every key row
     const int h = warp / 4;
     const int lane_base = (warp % 4) * 32;
@@ -477,11 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < 12) {
+  } else {
     // ------------------------------------------------------------------ dQ warpgroup
-    // Each dQ tile leaves TMEM in two halves of D/2 columns; a half is written, one row per
+    // Each dQ tile leaves TMEM in one round trip (the whole row of D FP32 columns into
+    // registers), so the columns go back to the MMA warp -- whose next dP^T product writes
+    // them -- as early as possible.  Then the tile is written in two halves, one row per
     // thread, into the 128B-swizzled staging boxes and pushed into the FP32 accumulator by
     // TMA reduce-adds issued by one thread (rows past N are dropped by the hardware).
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegDQ));
     const int lane_base = (warp % 4) * 32;
     const int r = lane_base + (threadIdx.x % 32);  // query row within the current query tile
     const bool leader = (r == 0);
@@ -492,28 +507,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&sh.dq_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
       const int q0 = (i0 + it) * kBlock;
+      uint32_t w[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(tDQ + c0, *reinterpret_cast<uint32_t(*)[32]>(w + c0));
+      tmem_ld_wait();
+      reg_fence(w);
+      tc_fence_before();
+      mbar_arrive(&sh.dq_empty);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t w[D / 2];
-#pragma unroll
-        for (int c0 = 0; c0 < D / 2; c0 += 32)
-          tmem_ld32(tDQ + half * (D / 2) + c0, *reinterpret_cast<uint32_t(*)[32]>(w + c0));
-        tmem_ld_wait();
-        reg_fence(w);
-        if (half == 1) {
-          // the whole tile is in registers: hand the columns back to the MMA warp
-          tc_fence_before();
-          mbar_arrive(&sh.dq_empty);
-        }
         // the staging boxes are free once the previous reductions have read them
         if (leader) bulk_wait_read_all();
         named_barrier(1, kBlock);
 #pragma unroll
         for (int b = 0; b < C::kDQBoxes; ++b)
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
+          for (int ch = 0; ch < 8; ++ch) {
+            const int c = half * (D / 2) + b * 32 + ch * 4;
             *reinterpret_cast<uint4*>(stage_row + b * 16384 + (((uint32_t)ch ^ sw) << 4)) =
-                make_uint4(w[b * 32 + ch * 4], w[b * 32 + ch * 4 + 1], w[b * 32 + ch * 4 + 2], w[b * 32 + ch * 4 + 3]);
+                make_uint4(w[c], w[c + 1], w[c + 2], w[c + 3]);
+          }
         fence_proxy_async_smem();
         named_barrier(1, kBlock);
         if (leader) {
@@ -613,6 +626,14 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if ((rc = check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                        "cudaFuncSetAttribute(bwd)")))
     return rc;
+  // setmaxnreg.inc waits until the block's launch registers cover the new split: refuse to
+  // launch a build whose launch allocation is smaller than the split needs
+  cudaFuncAttributes attr;
+  if ((rc = check_cuda(cudaFuncGetAttributes(&attr, kern), "cudaFuncGetAttributes(bwd)"))) return rc;
+  constexpr int kSplit = 2 * 128 * bwd::kRegPdS + 128 * bwd::kRegDQ + 128 * bwd::kRegOther;
+  if (attr.numRegs * bwd::kThreads < kSplit)
+    return set_error(FA_ERR_CUDA, "backward kernel built with %d registers/thread; its register split needs %d",
+                     attr.numRegs, (kSplit + bwd::kThreads - 1) / bwd::kThreads);
   kern<<<(unsigned)(p.n_tiles * p.BH), bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_main"))) return rc;
   }

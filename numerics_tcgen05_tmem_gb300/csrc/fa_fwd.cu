@@ -314,12 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nb; ++j) {
       if (!(ok = mbar_wait(&sh.s_full[t], j & 1, abort_flag, p.status))) break;
       tc_fence_after();
-      // the whole 128-column row in one round trip: four loads, one wait
+      // the whole 128-column row in one round trip: four loads, one wait; each load also
+      // returns the largest of its 32 raw scores
       uint32_t raw[kBlockN];
+      float pmax[kBlockN / 32];
 #pragma unroll
-      for (int c0 = 0; c0 < kBlockN; c0 += 32) tmem_ld32(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(raw + c0));
+      for (int c0 = 0; c0 < kBlockN; c0 += 32)
+        tmem_ld32_max(tS + c0, *reinterpret_cast<uint32_t(*)[32]>(raw + c0), pmax[c0 / 32]);
       tmem_ld_wait();
       reg_fence(raw);
+      reg_fence(pmax);
       float sv[kBlockN];
 #pragma unroll
       for (int i = 0; i < kBlockN; ++i) sv[i] = __uint_as_float(raw[i]);
@@ -330,18 +334,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kBlockN; ++i) sv[i] = (i < lim) ? sv[i] : -INFINITY;
       }
-      // block max with 3-input max over four independent chains
-      float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+      // block max: from the loads' reductions when no row of the warp has a masked column,
+      // else over the masked values with 3-input max in four independent chains
+      float bm;
+      if (__all_sync(0xffffffffu, lim >= kBlockN)) {
+        bm = fmaxf(max3f(pmax[0], pmax[1], pmax[2]), pmax[3]);
+      } else {
+        float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-      for (int i = 4; i < kBlockN - 4; i += 8) {
-        mx0 = max3f(mx0, sv[i], sv[i + 1]);
-        mx1 = max3f(mx1, sv[i + 2], sv[i + 3]);
-        mx2 = max3f(mx2, sv[i + 4], sv[i + 5]);
-        mx3 = max3f(mx3, sv[i + 6], sv[i + 7]);
+        for (int i = 4; i < kBlockN - 4; i += 8) {
+          mx0 = max3f(mx0, sv[i], sv[i + 1]);
+          mx1 = max3f(mx1, sv[i + 2], sv[i + 3]);
+          mx2 = max3f(mx2, sv[i + 4], sv[i + 5]);
+          mx3 = max3f(mx3, sv[i + 6], sv[i + 7]);
+        }
+        mx0 = max3f(mx0, sv[kBlockN - 4], sv[kBlockN - 3]);
+        mx1 = max3f(mx1, sv[kBlockN - 2], sv[kBlockN - 1]);
+        bm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       }
-      mx0 = max3f(mx0, sv[kBlockN - 4], sv[kBlockN - 3]);
-      mx1 = max3f(mx1, sv[kBlockN - 2], sv[kBlockN - 1]);
-      const float bm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       if constexpr (kStats) {
         // masked entries hold -inf; they never count as the row's minimum
         float mn0 = INFINITY, mn1 = INFINITY;
