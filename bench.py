@@ -320,6 +320,21 @@ def run_native(args):
     e2e_ms = max_over_ranks(e2e_run(E) / E, dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+
+    def link_gbs(dst, src, reps=5):
+        # one pinned copy alone on the copy stream: the host link's bandwidth on this machine
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(s_in):
+            dst.copy_(src, non_blocking=True)
+            ev[0].record(s_in)
+            for _ in range(reps):
+                dst.copy_(src, non_blocking=True)
+            ev[1].record(s_in)
+        torch.cuda.synchronize()
+        return src.numel() * src.element_size() * reps / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+
+    link_h2d = link_gbs(dev_in[0][0], host[0])
+    link_d2h = link_gbs(host_out[0][0], dev_out[0][0])
     binding.device_status(stream)
     for a_, b_ in zip((o, dq, dk, dv), (host_out[(E - 1) % 2][0], host_out[(E - 1) % 2][2], host_out[(E - 1) % 2][3],
                                          host_out[(E - 1) % 2][4])):
@@ -385,7 +400,9 @@ def run_native(args):
                       "bwd_dq_convert": round(conv_ms, 4)},
         "e2e": {"value": round(job_throughput(ff + fb, world, e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "steps": E, "pipelining": "copy-in, compute and copy-out streams, double-buffered device buffers"},
+                "steps": E, "pipelining": "copy-in, compute and copy-out streams, double-buffered device buffers",
+                "link_gbs": {"h2d": round(link_h2d, 1), "d2h": round(link_d2h, 1),
+                             "note": "one 67 MB pinned copy alone; bounds e2e at (h2d + d2h bytes) / bandwidth"}},
         "fp8_forward": {
             "kernel": "fa_fwd_kernel<128,stable,fp8>", "tflops": round(ff / (fp8_ms * 1e-3) / 1e12, 1),
             "ms": round(fp8_ms, 4), "launches_timed": R8,
