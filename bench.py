@@ -446,6 +446,67 @@ def run_profile_case(args):
     print("profile case ok", flush=True)
 
 
+# --------------------------------------------------------------------------- every workload
+def run_configs(args):
+    """Forward (plain and stabilised) and backward time of each workload: one JSON line each.
+
+    CUDA events around R launches after 3 warm-ups; the GPT-2-sized inputs fit in L2, so a
+    256 MB buffer is rewritten between launches to flush it (the 8k/16k inputs exceed L2).
+    """
+    import torch
+
+    from numerics_tcgen05_tmem_gb300 import binding, build, inputs
+
+    build.build()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    peak = load_peaks()["bf16_tflops"]
+    cases = [("tiny_ties", inputs.tiny_ties()), ("gpt2_small", inputs.gpt2_small()),
+             ("gpt2_medium_sink", inputs.gpt2_medium_sink()), ("llama7b_long", inputs.llama7b_long()),
+             ("extreme_16k_causal", inputs.extreme_16k()), ("extreme_16k_noncausal", inputs.extreme_16k(causal=False))]
+    R = 10
+    for name, w in cases:
+        q, k, v, do = (t.to("cuda") for t in (w.q, w.k, w.v, w.do))
+        B, H, N, d = q.shape
+        small = q.numel() * 2 * 4 < 129e6
+        ws = torch.empty(binding.fa_bwd_workspace_size(B, H, N, d), device="cuda", dtype=torch.uint8)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            tot = 0.0
+            for _ in range(R):
+                if small:
+                    flush.zero_()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                e[0].record()
+                fn()
+                e[1].record()
+                e[1].synchronize()
+                tot += e[0].elapsed_time(e[1])
+            return tot / R
+
+        ff = flops_fwd(B, H, N, d, w.causal)
+        line = {"workload": name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal, "scale": w.scale,
+                "l2_flush": small}
+        for stable in (0, 1):
+            ms = timed(lambda: binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=stable, beta=w.beta))
+            line[f"fwd_stable{stable}_ms"] = round(ms, 4)
+            line[f"fwd_stable{stable}_tflops"] = round(ff / (ms * 1e-3) / 1e12, 1)
+        o, lse = binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=1, beta=w.beta)
+        ms = timed(lambda: binding.backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, workspace=ws))
+        line["bwd_ms"] = round(ms, 4)
+        line["bwd_tflops"] = round(2.5 * ff / (ms * 1e-3) / 1e12, 1)
+        line["fwd_stable1_frac_of_peak"] = round(line["fwd_stable1_tflops"] / peak, 4)
+        line["bwd_frac_of_peak"] = round(line["bwd_tflops"] / peak, 4)
+        # HBM view of the forward: Q, K, V read and O written once, plus the LSE
+        line["fwd_stable1_hbm_gbs"] = round((4 * q.numel() * 2 + B * H * N * 4) / (line["fwd_stable1_ms"] * 1e-3) / 1e9, 1)
+        binding.device_status()
+        print(json.dumps(line), flush=True)
+        del q, k, v, do, o, lse, ws
+        torch.cuda.empty_cache()
+
+
 # --------------------------------------------------------------------------- reference arm (the oracle)
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -484,11 +545,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--configs", action="store_true",
+                    help="time forward and backward of every workload (one JSON line each) and exit")
     ap.add_argument("--profile-case", action="store_true",
                     help="run each kernel once on an 8-head slice (for ncu captures) and exit")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
+        return
+    if args.configs:
+        run_configs(args)
         return
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3
