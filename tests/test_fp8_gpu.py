@@ -175,3 +175,24 @@ def test_nonfinite_descale_is_reported():
     assert binding.fa_device_status() == binding.FA_WARN_NONFINITE
     assert binding.fa_fwd_fp8(q8, k8, v8, torch.from_numpy(ds).cuda(), o, lse, True, w.scale, 1, 1.25) == binding.FA_OK
     assert binding.fa_device_status() == binding.FA_OK
+
+
+@pytest.mark.parametrize("beta", [1.1, 1.5])
+def test_sink_other_betas(beta):
+    w = inputs.gpt2_medium_sink(B=1, H=2, N=640, d=128)
+    codes, ds = oracle_quantized(w)
+    o, lse, st = run_fp8(codes, ds, w, 1, beta=beta)
+    ref = F.forward_fp8(*codes, ds, w.scale, True, stable=1, beta=beta)
+    assert rel_fro(o, ref["o"]) <= FP8_REL_TOL
+    assert_lse(lse, ref["lse"])
+    assert np.mean(st["row_branch"].cpu().numpy() == ref["branch"]) > 0.999
+
+
+def test_extreme_16k_noncausal_sampled_head():
+    w = inputs.extreme_16k(causal=False)
+    codes, ds = oracle_quantized(w)
+    o, lse = run_fp8(codes, ds, w, 1, stats=False)
+    sub = [c[:, [7]] for c in codes]
+    ref = F.forward_fp8(*sub, ds, w.scale, False, stable=1, beta=w.beta)
+    assert rel_fro(o[:, [7]], ref["o"]) <= FP8_REL_TOL
+    assert_lse(lse[:, [7]], ref["lse"])

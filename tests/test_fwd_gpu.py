@@ -217,3 +217,13 @@ def test_nonfinite_outputs_are_reported():
     v[0, 1, 7, 3] = 0.0
     assert binding.fa_fwd(q, k, v, o, lse, True, w.scale, 1, 1.25) == binding.FA_OK
     assert binding.fa_device_status() == binding.FA_OK
+
+
+def test_longest_sequence_sampled_head():
+    # 32k tokens (the largest size tested): one head checked against the oracle in full
+    w = inputs.random_case(1, 2, 32768, 128, True, seed=321, std=1.0)
+    o, lse = run_fwd(w, 1, stats=False)
+    sub = inputs.Workload("sub", w.q[:, 1:], w.k[:, 1:], w.v[:, 1:], w.do[:, 1:], True, w.scale, 1, 1.25)
+    ref = A.forward(sub.q, sub.k, sub.v, w.scale, True, stable=1, beta=1.25, row_block=256)
+    assert_close_bf16("o", o[:, 1:], ref["o"])
+    assert_lse(lse[:, 1:], ref["lse"])
