@@ -29,6 +29,7 @@
 // Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV.
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -77,6 +78,7 @@ struct Bars {
   uint64_t kv_full;
   uint64_t q_full[kStages], q_empty[kStages], do_full, do_empty;
   uint64_t s_full, p_ready, dp_full, ds_ready, ds_empty, dq_full, dq_empty, mma_done;
+  uint64_t never;  // test builds only: a barrier nothing arrives on
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -95,6 +97,7 @@ struct Params {
   int causal;
   float scale;
   float scale_log2;
+  int inject_stall;  // test builds only (FA_TEST_HOOKS): make the MMA warp's first wait run out
 };
 
 // --------------------------------------------------------------------------- preprocess
@@ -208,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_empty, kBlock);
     mbar_init(&sh.mma_done, 1);
+    mbar_init(&sh.never, 1);
     fence_barrier_init();
   }
   if (warp == kMmaWarp) {
@@ -273,6 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MN-major operand with 128 K rows: 2 KB per k-step, 16 KB between 64-column blocks
       auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, 16384, 1024); };
       bool ok = mbar_wait(&sh.kv_full, 0, abort_flag, p.status);
+#ifdef FA_TEST_HOOKS
+      // failure-detection test: wait on a barrier nothing arrives on; the bounded wait runs
+      // out, raises the CTA's abort flag and records a timeout, and every warp unwinds
+      if (p.inject_stall) ok = ok && mbar_wait(&sh.never, 0, abort_flag, p.status);
+#endif
       auto issue_s = [&](int it) {  // S^T = K_j Q_i^T
         const int s = it % kStages;
         if (!(ok = mbar_wait(&sh.q_full[s], (it / kStages) & 1, abort_flag, p.status))) return;
@@ -622,6 +631,10 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   p.causal = causal;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+#ifdef FA_TEST_HOOKS
+  const char* inject = getenv("FA_TEST_INJECT_STALL");
+  p.inject_stall = (inject && inject[0] == '1') ? 1 : 0;
+#endif
   auto kern = bwd::fa_bwd_main<D>;
   if ((rc = check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                        "cudaFuncSetAttribute(bwd)")))
