@@ -90,3 +90,45 @@ def test_bf16_emulation_within_contract_tolerance():
     rel = np.linalg.norm(em["o"] - ref["o"]) / np.linalg.norm(ref["o"])
     assert rel <= 1e-2
     assert np.max(np.abs(em["lse"] - ref["lse"])) <= 1e-3
+
+
+def test_block_local_variant_with_one_block_is_the_whole_row_rule():
+    # stable = 2 with a single key block: m = max(-inf, rule(bm, bc)) = rule(rm, rs)
+    w = inputs.tiny_ties(N=128)
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, beta=w.beta)
+    em2 = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=2, beta=w.beta, block_n=128)
+    em1 = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, beta=w.beta, block_n=128)
+    np.testing.assert_array_equal(em2["branch"], ref["branch"])
+    np.testing.assert_array_equal(em2["m"], em1["m"])
+    np.testing.assert_array_equal(em2["ones"], em1["ones"])
+
+
+def test_block_local_shift_is_the_running_max_of_block_rules():
+    # brute force on FP64 scores (exact for dyadic inputs): per block, the rule applied to
+    # that block's own maximum and tie count; the row keeps the largest shift, and the branch
+    # of the latest block whose shift is at least the previous one
+    w = inputs.tiny_ties(N=300, H=2)
+    q, k = w.q.double().numpy(), w.k.double().numpy()
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, w.causal, stable=2, beta=w.beta, block_n=128)
+    beta32 = np.float32(w.beta)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            s = q[b, h] @ k[b, h].T
+            for i in range(q.shape[2]):
+                m, br = -np.inf, 0
+                for j0 in range(0, i + 1, 128):
+                    blk = s[i, j0:min(i + 1, j0 + 128)]
+                    bm = blk.max()
+                    bc = int((blk == bm).sum())
+                    if bc > 1 and bm > 0:
+                        mb, brb = float(np.float32(beta32 * np.float32(bm))), 1
+                    elif bc > 1 and bm < 0:
+                        mb, brb = 0.0, 2
+                    else:
+                        mb, brb = bm, 0
+                    if mb >= m:
+                        br = brb
+                    m = max(m, mb)
+                assert em["m"][b, h, i] == np.float32(m), (b, h, i)
+                assert em["branch"][b, h, i] == br, (b, h, i)
+    assert (em["branch"] != 0).sum() > 0
