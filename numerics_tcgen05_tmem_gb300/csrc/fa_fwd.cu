@@ -12,7 +12,10 @@
 // evaluated with selects (no divergent branch) after every block.
 // Precision (jsqmd.com "Flash Attention低精度训练稳定性优化实践" §3.2): QK^T and
 // P~V accumulate in FP32 (TMEM), the softmax runs in FP32, P~ is rounded to BF16
-// (round-to-nearest-even) for the P~V product.
+// (round-to-nearest-even) for the P~V product; l is summed with Kahan compensation
+// across key blocks (ijyty.com §7.2).
+// FP8 variant (ijyty.com §6.1, FP8 with dynamic scaling): E4M3 Q, K, V with per-tensor
+// scales folded into the exponent's factor, kind::f8f6f4 MMAs, P~ * 2^8 rounded to E4M3.
 //
 // CTA organisation (one CTA = two 128-row query tiles of one (b, h)), 512 threads:
 //   warps 0-3   softmax warpgroup for tile 0 (thread = one query row = one TMEM lane)
@@ -23,8 +26,9 @@
 // Registers are rebalanced after the launch (setmaxnreg): softmax threads hold a whole
 // 128-column row of S, the others need few.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1; the BF16 P~ of a tile is written
-// over the first 64 columns of its S (each thread has read its own S row first)
-// and fed to the P~V MMA straight from TMEM.
+// over the first 64 columns of its S (32 for E4M3; each thread has read its own S row
+// first) and fed to the P~V MMA straight from TMEM.  The row's block maximum comes with
+// the TMEM load of S (tcgen05.ld.red.max) whenever the block has no masked column.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdio.h>
