@@ -137,3 +137,10 @@ def test_longest_sequence_sampled_head():
     res = run_fwd_bwd(w)
     sub = inputs.Workload("sub", w.q[:, :1], w.k[:, :1], w.v[:, :1], w.do[:, :1], True, w.scale, 1, 1.25)
     check(sub, res, oracle_grads(sub), sel=lambda t: t[:, :1])
+
+
+@pytest.mark.parametrize("scale", [0.01, 1.0])
+def test_unusual_scales(scale):
+    w = inputs.random_case(1, 2, 700, 128, True, seed=int(scale * 1000) + 4, std=1.0)
+    w = inputs.Workload("scaled", w.q, w.k, w.v, w.do, True, scale, 1, 1.25)
+    check(w, run_fwd_bwd(w), oracle_grads(w))

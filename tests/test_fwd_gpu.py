@@ -227,3 +227,24 @@ def test_longest_sequence_sampled_head():
     ref = A.forward(sub.q, sub.k, sub.v, w.scale, True, stable=1, beta=1.25, row_block=256)
     assert_close_bf16("o", o[:, 1:], ref["o"])
     assert_lse(lse[:, 1:], ref["lse"])
+
+
+@pytest.mark.parametrize("beta", [1.0, 2.0])
+def test_beta_at_and_beyond_the_recommended_range(beta):
+    # beta = 1 makes the positive branch m = rm (the plain shift); beta = 2 moves it far
+    w = inputs.gpt2_medium_sink(B=2, H=2, N=512)
+    o, lse, st = run_fwd(w, 1, beta)
+    ref = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, beta=beta)
+    assert_close_bf16("o", o, ref["o"])
+    assert_lse(lse, ref["lse"])
+    assert np.mean(st["row_branch"].cpu().numpy() == ref["branch"]) > 0.999
+
+
+@pytest.mark.parametrize("scale", [0.01, 1.0])
+def test_unusual_scales(scale):
+    w = inputs.random_case(1, 2, 700, 128, True, seed=int(scale * 1000) + 3, std=1.0)
+    w = inputs.Workload("scaled", w.q, w.k, w.v, w.do, True, scale, 1, 1.25)
+    o, lse = run_fwd(w, 1, stats=False)
+    ref = A.forward(w.q, w.k, w.v, scale, True, stable=1, beta=1.25)
+    assert_close_bf16("o", o, ref["o"])
+    assert_lse(lse, ref["lse"])
