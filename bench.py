@@ -150,10 +150,13 @@ def cpu_cores():
     return os.cpu_count()
 
 
+CPU_BASELINE_HEADS = 8  # about 10-20 s of oracle work on the host cores
+
+
 def cpu_baseline():
-    fl, dt = oracle_sample_run(1)
+    fl, dt = oracle_sample_run(CPU_BASELINE_HEADS)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": "1 of 32 heads (N=8192, d=128, causal) forward + backward, numpy FP64; "
+            "sample": f"{CPU_BASELINE_HEADS} of 32 heads (N=8192, d=128, causal) forward + backward, numpy FP64; "
                       f"{dt:.1f} s for {fl / 1e9:.0f} GFLOP"}
 
 
