@@ -71,12 +71,27 @@ struct Cfg {
   static constexpr int kKOff = kQOff + kTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kVOff + kStages * kTileBytes + 1024;  // +1024 for alignment
-  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + D;
+  // d = 64 leaves 128 TMEM columns beside S0 | S1 | O0 | O1: a third S buffer.  The S of
+  // (tile t, block j) then goes to buffer (2j + t) mod 3, so a tile's next S can be computed
+  // while its softmax still works on the current one.
+  static constexpr bool kRing = (D == 64) && !kFp8;
+  static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
+  static constexpr uint32_t kTmemO0 = kRing ? 384 : 256, kTmemO1 = kTmemO0 + D;
+  __device__ static uint32_t s_col(int t, int j) {
+    return kRing ? (uint32_t)(((2 * j + t) % 3) * 128) : (t == 0 ? kTmemS0 : kTmemS1);
+  }
   // Q K^T with both operands K-major; P~ (TMEM) x V with V MN-major
   static constexpr uint32_t kIdescS = kFp8 ? idesc_e4m3(128, kBlockN, false, false) : idesc_bf16(128, kBlockN, false, false);
   static constexpr uint32_t kIdescO = kFp8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
   static_assert(kAtoms >= 1, "a tile row must fill at least one 128-byte swizzle atom");
 };
+
+// Barrier slot and wait parity of hand-off event e (see Shared): two alternating barriers
+// with the d = 64 ring, one barrier otherwise.
+template <bool kTwo>
+__device__ __forceinline__ int ev_slot(int e) { return kTwo ? (e & 1) : 0; }
+template <bool kTwo>
+__device__ __forceinline__ uint32_t ev_parity(int e) { return kTwo ? (uint32_t)((e >> 1) & 1) : (uint32_t)(e & 1); }
 
 struct Params {
   __nv_bfloat16* o;
@@ -101,8 +116,14 @@ struct Params {
 struct Shared {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t s_full[kTiles], p_ready[kTiles], pv_done[kTiles];
-  uint64_t alpha_ready[kTiles], o_ready[kTiles], l_ready[kTiles];
+  // Hand-offs that can run two events ahead of their waiter (with the d = 64 ring a tile's
+  // softmax may finish two blocks before the MMA warp takes the first) use two barriers
+  // per tile: event e lands on [e & 1] and is awaited with parity (e >> 1) & 1, so neither
+  // barrier runs more than one phase ahead.  Without the ring only [0] is used, with
+  // parity e & 1.  Events: S and P~ of block j (e = j); alpha and the corrected O of
+  // block j >= 1 (e = j - 1).
+  uint64_t s_full[kTiles][2], p_ready[kTiles][2], pv_done[kTiles];
+  uint64_t alpha_ready[kTiles][2], o_ready[kTiles][2], l_ready[kTiles];
   uint64_t mma_done;
   uint64_t never;  // test builds only: a barrier nothing arrives on
   float alpha[kTiles][kBlockM];  // correction factor of each row for the current block
@@ -152,11 +173,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.v_empty[s], 1);
     }
     for (int t = 0; t < kTiles; ++t) {
-      mbar_init(&sh.s_full[t], 1);
-      mbar_init(&sh.p_ready[t], kBlockM);
+      mbar_init(&sh.s_full[t][0], 1);
+      mbar_init(&sh.s_full[t][1], 1);
+      mbar_init(&sh.p_ready[t][0], kBlockM);
+      mbar_init(&sh.p_ready[t][1], kBlockM);
       mbar_init(&sh.pv_done[t], 1);
-      mbar_init(&sh.alpha_ready[t], kBlockM);
-      mbar_init(&sh.o_ready[t], kBlockM);
+      mbar_init(&sh.alpha_ready[t][0], kBlockM);
+      mbar_init(&sh.alpha_ready[t][1], kBlockM);
+      mbar_init(&sh.o_ready[t][0], kBlockM);
+      mbar_init(&sh.o_ready[t][1], kBlockM);
       mbar_init(&sh.l_ready[t], kBlockM);
     }
     mbar_init(&sh.mma_done, 1);
@@ -229,9 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
       tc_fence_after();
       // S_t = Q_t K_j^T over D/16 k-steps (K-major SW128 operands, 16 KB per 64 columns)
-      auto issue_s = [&](int t, int s) {
+      auto issue_s = [&](int t, int s, int j) {
         const uint32_t a0 = sQ + t * C::kTileBytes, b0 = sK + s * C::kTileBytes;
-        const uint32_t d = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1);
+        const uint32_t d = tmem + C::s_col(t, j);
 #pragma unroll
         for (int kk = 0; kk < C::kKStepsS; ++kk) {
           const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -240,14 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::kIdescS, kk > 0);
         }
-        tc_commit(&sh.s_full[t]);
+        tc_commit(&sh.s_full[t][ev_slot<C::kRing>(j)]);
       };
       // O_t += P~_t V_j: P~ from TMEM (K = 128 keys, 8 columns = 32 bytes per k-step), V MN-major
       // (a k-step covers 32 / kElem keys of 128-byte rows)
       auto issue_pv = [&](int t, int s, int j) {
         const uint32_t b0 = sV + s * C::kTileBytes;
         const uint32_t d = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1);
-        const uint32_t a = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1);
+        const uint32_t a = tmem + C::s_col(t, j);
 #pragma unroll
         for (int kk = 0; kk < C::kKStepsO; ++kk) {
           const uint64_t bd = sdesc_sw128(b0 + kk * (32 / C::kElem) * 128, 16384, 1024);
@@ -258,32 +283,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(&sh.pv_done[t]);
       };
-      // Order: S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 PV1_1 S1_2 | ... | PV0_last PV1_last
-      for (int j = 0; ok && j <= nbmax; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = (j / C::kStages) & 1;
-        const int sp = (j + C::kStages - 1) % C::kStages;  // stage of block j-1
-        if (j < nbmax) {
-          if (!(ok = mbar_wait(&sh.k_full[s], ph, abort_flag, p.status))) break;
+      if constexpr (C::kRing) {
+        // Order: S0_0 S1_0 S0_1 | PV0_0 S1_1 PV1_0 S0_2 | PV0_1 S1_2 PV1_1 S0_3 | ...
+        // S(t, j) writes buffer (2j + t) mod 3, whose previous user's P~V is always issued
+        // before it (same-thread MMAs run in order), and each P~V follows its softmax.
+        int k_ready = -1;  // K blocks up to this one have landed
+        auto need_k = [&](int b) {
+          if (b <= k_ready) return true;
+          if (!(ok = mbar_wait(&sh.k_full[b % C::kStages], (b / C::kStages) & 1, abort_flag, p.status))) return false;
           tc_fence_after();
+          k_ready = b;
+          return true;
+        };
+        auto pv_when_ready = [&](int t, int b) {  // P~V of (tile t, block b) once P~ and O are ready
+          if (!(ok = mbar_wait(&sh.p_ready[t][ev_slot<true>(b)], ev_parity<true>(b), abort_flag, p.status))) return;
+          if (b > 0 &&
+              !(ok = mbar_wait(&sh.o_ready[t][ev_slot<true>(b - 1)], ev_parity<true>(b - 1), abort_flag, p.status)))
+            return;
+          tc_fence_after();
+          issue_pv(t, b % C::kStages, b);
+        };
+        if (nbmax > 0 && need_k(0)) {
+          for (int t = 0; t < kTiles; ++t)
+            if (nb[t] > 0) issue_s(t, 0, 0);
+          tc_commit(&sh.k_empty[0]);
+          if (nb[0] > 1 && need_k(1)) issue_s(0, 1, 1);
         }
-        if (j > 0) {
+        for (int j = 1; ok && j <= nbmax; ++j) {
+          const int sp = (j - 1) % C::kStages;  // stage of block j-1
           if (!(ok = mbar_wait(&sh.v_full[sp], ((j - 1) / C::kStages) & 1, abort_flag, p.status))) break;
           tc_fence_after();
-        }
-        for (int t = 0; t < kTiles; ++t) {
-          if (j > 0 && j - 1 < nb[t]) {
-            if (!(ok = mbar_wait(&sh.p_ready[t], (j - 1) & 1, abort_flag, p.status))) break;
-            // O_t must carry block j-1's correction (applied by the correction warpgroup)
-            if (j - 1 > 0 && !(ok = mbar_wait(&sh.o_ready[t], (j - 2) & 1, abort_flag, p.status))) break;
-            tc_fence_after();
-            issue_pv(t, sp, j - 1);
+          if (j - 1 < nb[0]) {
+            pv_when_ready(0, j - 1);
+            if (!ok) break;
           }
-          if (j < nb[t]) issue_s(t, s);
+          if (j < nb[1]) {
+            if (!need_k(j)) break;
+            issue_s(1, j % C::kStages, j);
+          }
+          if (j < nbmax) tc_commit(&sh.k_empty[j % C::kStages]);  // S(0, j) and S(1, j) issued
+          if (j - 1 < nb[1]) {
+            pv_when_ready(1, j - 1);
+            if (!ok) break;
+          }
+          tc_commit(&sh.v_empty[sp]);
+          if (j + 1 < nb[0]) {
+            if (!need_k(j + 1)) break;
+            issue_s(0, (j + 1) % C::kStages, j + 1);
+          }
         }
-        if (!ok) break;
-        if (j < nbmax) tc_commit(&sh.k_empty[s]);
-        if (j > 0) tc_commit(&sh.v_empty[sp]);
+      } else {
+        // Order: S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 PV1_1 S1_2 | ... | PV0_last PV1_last
+        for (int j = 0; ok && j <= nbmax; ++j) {
+          const int s = j % C::kStages;
+          const uint32_t ph = (j / C::kStages) & 1;
+          const int sp = (j + C::kStages - 1) % C::kStages;  // stage of block j-1
+          if (j < nbmax) {
+            if (!(ok = mbar_wait(&sh.k_full[s], ph, abort_flag, p.status))) break;
+            tc_fence_after();
+          }
+          if (j > 0) {
+            if (!(ok = mbar_wait(&sh.v_full[sp], ((j - 1) / C::kStages) & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+          }
+          for (int t = 0; t < kTiles; ++t) {
+            if (j > 0 && j - 1 < nb[t]) {
+              if (!(ok = mbar_wait(&sh.p_ready[t][0], ev_parity<false>(j - 1), abort_flag, p.status))) break;
+              // O_t must carry block j-1's correction (applied by the correction warpgroup)
+              if (j - 1 > 0 && !(ok = mbar_wait(&sh.o_ready[t][0], ev_parity<false>(j - 2), abort_flag, p.status)))
+                break;
+              tc_fence_after();
+              issue_pv(t, sp, j - 1);
+            }
+            if (j < nb[t]) issue_s(t, s, j);
+          }
+          if (!ok) break;
+          if (j < nbmax) tc_commit(&sh.k_empty[s]);
+          if (j > 0) tc_commit(&sh.v_empty[sp]);
+        }
       }
       // every MMA issued above has completed before TMEM is released
       tc_commit(&sh.mma_done);
@@ -302,7 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = lane_base + (threadIdx.x % 32);  // row within the tile
     const int nb = (t == 0) ? nb0 : nb1;
     const int row = qb * (kTiles * kBlockM) + t * kBlockM + r;
-    const uint32_t tS = tmem + (t == 0 ? C::kTmemS0 : C::kTmemS1) + ((uint32_t)lane_base << 16);
+    const uint32_t lane_off = (uint32_t)lane_base << 16;
+    const uint32_t tS_fixed = tmem + C::s_col(t, 0) + lane_off;  // without the ring: S0 or S1
     // FP8: raw scores are in units of dq * dk (the Q and K scales); fold both into the
     // exponent's scale.  rm, m and the tie count stay in accumulator units, which is the same
     // rule on the dequantised scores (a positive factor keeps order, equality and sign).
@@ -316,8 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int branch = 0;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
-      if (!(ok = mbar_wait(&sh.s_full[t], j & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.s_full[t][ev_slot<C::kRing>(j)], ev_parity<C::kRing>(j), abort_flag, p.status))) break;
       tc_fence_after();
+      const uint32_t tS = C::kRing ? tmem + C::s_col(t, j) + lane_off : tS_fixed;  // this block's S, then P~
       // the whole 128-column row in one round trip: four loads, one wait; each load also
       // returns the largest of its 32 raw scores
       uint32_t raw[kBlockN];
@@ -407,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j > 0) {
         // hand the row's correction factor to the correction warpgroup right away
         sh.alpha[t][r] = alpha;
-        mbar_arrive(&sh.alpha_ready[t]);
+        mbar_arrive(&sh.alpha_ready[t][ev_slot<C::kRing>(j - 1)]);
       }
       // FP8: P~ * 2^8 (added to the exponent) uses the E4M3 range below 448 instead of <= 1
       const float nmc = kFp8 ? fmaf(-m_new, c, (float)kPScaleLog2) : -m_new * c;
@@ -471,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sh.p_ready[t]);
+      mbar_arrive(&sh.p_ready[t][ev_slot<C::kRing>(j)]);
       m = m_new;
     }
     // ------------------------------------------------------------ row results
@@ -507,7 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 1; ok && j < nbmax; ++j) {
       for (int t = 0; t < kTiles; ++t) {
         if (j >= nb[t]) continue;
-        if (!(ok = mbar_wait(&sh.alpha_ready[t], (j - 1) & 1, abort_flag, p.status))) break;
+        if (!(ok = mbar_wait(&sh.alpha_ready[t][ev_slot<C::kRing>(j - 1)], ev_parity<C::kRing>(j - 1), abort_flag,
+                             p.status)))
+          break;
         const float alpha = sh.alpha[t][r];
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           // the previous P~V of this tile has landed (its S_j commit already implies it)
@@ -532,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
         }
         tc_fence_before();
-        mbar_arrive(&sh.o_ready[t]);
+        mbar_arrive(&sh.o_ready[t][ev_slot<C::kRing>(j - 1)]);
       }
     }
     // ------------------------------------------------------------ epilogue: O = O / l -> BF16

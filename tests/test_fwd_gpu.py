@@ -248,3 +248,20 @@ def test_unusual_scales(scale):
     ref = A.forward(w.q, w.k, w.v, scale, True, stable=1, beta=1.25)
     assert_close_bf16("o", o, ref["o"])
     assert_lse(lse, ref["lse"])
+
+
+@pytest.mark.parametrize("stable", [0, 1, 2])
+def test_repeated_launches_without_stats(stable):
+    # back-to-back launches of the plain-output kernels (their hand-offs run at full speed):
+    # every launch completes without a timeout and gives the same bits as the first
+    w = inputs.gpt2_small()
+    q, k, v, _ = to_dev(w)
+    first = None
+    for _ in range(6):
+        o, lse = binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=stable, beta=w.beta)
+        if first is None:
+            first = (o, lse)
+    binding.device_status()
+    assert torch.equal(o, first[0]) and torch.equal(lse, first[1])
+    ref = A.forward(w.q[:1], w.k[:1], w.v[:1], w.scale, True, stable=stable if stable < 2 else 0, beta=w.beta)
+    assert_close_bf16("o", o[:1], ref["o"])
