@@ -126,7 +126,7 @@ int fa_quantize_fp8(const void* x, size_t n, void* x8, float* descale, void* str
  *   dequantised scores (q8 dq).(k8 dk); P~ is multiplied by 2^8 and rounded to E4M3 for the
  *   P~V product; stats->row_max_raw / row_min_raw are in dequantised units and
  *   stats->row_ones counts P~ entries whose E4M3 value is exactly 1.0 (2^8 after scaling).
- *   d must be 128 (FA_ERR_UNSUPPORTED otherwise).
+ *   d must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
  * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA.
  */
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale, void* o, float* lse,

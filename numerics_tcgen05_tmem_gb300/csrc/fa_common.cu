@@ -66,7 +66,7 @@ int sm_count() {
 }
 
 static int encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, int BH, int N,
-                     int d, int box_cols, int box_rows) {
+                     int d, int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_encode) {
@@ -83,7 +83,7 @@ static int encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes
   cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return FA_OK;
 }
@@ -93,7 +93,9 @@ int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int
 }
 
 int make_tmap_u8_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
-  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, BH, N, d, 128, box_rows);
+  // one swizzle atom per row: 128-byte rows (d = 128) or 64-byte rows (d = 64)
+  if (d >= 128) return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, BH, N, d, 128, box_rows);
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, BH, N, d, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int make_tmap_f32_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {

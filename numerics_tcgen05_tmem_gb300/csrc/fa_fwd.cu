@@ -62,8 +62,12 @@ struct Cfg {
   static constexpr int kElem = kFp8 ? 1 : 2;                // bytes per Q/K/V element
   static constexpr int kStages = kFp8 ? 4 : ((D == 128) ? 2 : 4);
   static constexpr int kTileBytes = kBlockM * D * kElem;    // one 128 x D tile (Q, K or V)
-  static constexpr int kAtoms = D * kElem / 128;            // 128-byte column blocks of a tile
-  static constexpr int kAtomElems = 128 / kElem;            // elements per 128-byte row of an atom
+  // Swizzle atom: 128-byte rows, or 64-byte rows when a tile row is only 64 bytes (E4M3, d = 64)
+  static constexpr int kAtomBytes = (D * kElem >= 128) ? 128 : 64;
+  static constexpr int kAtoms = D * kElem / kAtomBytes;     // atom column blocks of a tile
+  static constexpr int kAtomElems = kAtomBytes / kElem;     // elements per atom row
+  static constexpr int kAtomBlock = kBlockM * kAtomBytes;   // bytes of one atom column block (128 rows)
+  static constexpr int kStepsPerAtom = kAtomBytes / 32;     // 32-byte k-steps per atom row
   static constexpr int kKStepsS = D * kElem / 32;           // Q K^T k-steps (32 bytes each)
   static constexpr int kKStepsO = kBlockN * kElem / 32;     // P~ V k-steps over the keys
   static constexpr int kPCols = kBlockN * kElem / 4;        // TMEM columns of a packed P~ row
@@ -74,7 +78,7 @@ struct Cfg {
   // d = 64 leaves 128 TMEM columns beside S0 | S1 | O0 | O1: a third S buffer.  The S of
   // (tile t, block j) then goes to buffer (2j + t) mod 3, so a tile's next S can be computed
   // while its softmax still works on the current one.
-  static constexpr bool kRing = (D == 64) && !kFp8;
+  static constexpr bool kRing = (D == 64);
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
   static constexpr uint32_t kTmemO0 = kRing ? 384 : 256, kTmemO1 = kTmemO0 + D;
   __device__ static uint32_t s_col(int t, int j) {
@@ -83,7 +87,11 @@ struct Cfg {
   // Q K^T with both operands K-major; P~ (TMEM) x V with V MN-major
   static constexpr uint32_t kIdescS = kFp8 ? idesc_e4m3(128, kBlockN, false, false) : idesc_bf16(128, kBlockN, false, false);
   static constexpr uint32_t kIdescO = kFp8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
-  static_assert(kAtoms >= 1, "a tile row must fill at least one 128-byte swizzle atom");
+  static_assert(kAtoms >= 1 && kAtoms * kAtomBytes == D * kElem, "tile rows must be whole swizzle atoms");
+  // shared-memory descriptor of an operand in this tile layout (8-row groups kAtomBytes * 8 apart)
+  __device__ static uint64_t sdesc(uint32_t saddr, uint32_t lbo) {
+    return kAtomBytes == 128 ? sdesc_sw128(saddr, lbo, 8 * kAtomBytes) : sdesc_sw64(saddr, lbo, 8 * kAtomBytes);
+  }
 };
 
 // Barrier slot and wait parity of hand-off event e (see Shared): two alternating barriers
@@ -210,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&sh.q_full, ntiles * C::kTileBytes);
       for (int t = 0; t < ntiles; ++t)
         for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * 16384, &tmQ, &sh.q_full, c * C::kAtomElems,
+          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * C::kAtomBlock, &tmQ, &sh.q_full, c * C::kAtomElems,
                       qb * (kTiles * kBlockM) + t * kBlockM, bh);
       int nk_issued = 0, nv_issued = 0;
       for (int j = 0; j < nbmax; ++j) {
@@ -219,13 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&sh.k_empty[s], ph ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&sh.k_full[s], C::kTileBytes);
         for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * 16384, &tmK, &sh.k_full[s], c * C::kAtomElems,
+          tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * C::kAtomBlock, &tmK, &sh.k_full[s], c * C::kAtomElems,
                       j * kBlockN, bh);
         nk_issued = j + 1;
         if (!mbar_wait(&sh.v_empty[s], ph ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&sh.v_full[s], C::kTileBytes);
         for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + c * 16384, &tmV, &sh.v_full[s], c * C::kAtomElems,
+          tma_load_3d(smem + C::kVOff + s * C::kTileBytes + c * C::kAtomBlock, &tmV, &sh.v_full[s], c * C::kAtomElems,
                       j * kBlockN, bh);
         nv_issued = j + 1;
       }
@@ -253,17 +261,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.inject_stall) ok = ok && mbar_wait(&sh.never, 0, abort_flag, p.status);
 #endif
       tc_fence_after();
-      // S_t = Q_t K_j^T over D/16 k-steps (K-major SW128 operands, 16 KB per 64 columns)
+      // S_t = Q_t K_j^T over 32-byte k-steps (K-major swizzled operands, one atom column
+      // block of 128 rows per kAtomBytes of each row)
       auto issue_s = [&](int t, int s, int j) {
         const uint32_t a0 = sQ + t * C::kTileBytes, b0 = sK + s * C::kTileBytes;
         const uint32_t d = tmem + C::s_col(t, j);
 #pragma unroll
         for (int kk = 0; kk < C::kKStepsS; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          const uint32_t off = (kk / C::kStepsPerAtom) * C::kAtomBlock + (kk % C::kStepsPerAtom) * 32;
           if constexpr (kFp8)
-            mma_ss_f8(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::kIdescS, kk > 0);
+            mma_ss_f8(d, C::sdesc(a0 + off, 16), C::sdesc(b0 + off, 16), C::kIdescS, kk > 0);
           else
-            mma_ss(d, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024), C::kIdescS, kk > 0);
+            mma_ss(d, C::sdesc(a0 + off, 16), C::sdesc(b0 + off, 16), C::kIdescS, kk > 0);
         }
         tc_commit(&sh.s_full[t][ev_slot<C::kRing>(j)]);
       };
@@ -275,7 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a = tmem + C::s_col(t, j);
 #pragma unroll
         for (int kk = 0; kk < C::kKStepsO; ++kk) {
-          const uint64_t bd = sdesc_sw128(b0 + kk * (32 / C::kElem) * 128, 16384, 1024);
+          // a k-step covers 32 / kElem keys, one atom row (kAtomBytes) each; LBO = the next
+          // atom column block along d (only with two or more)
+          const uint64_t bd = C::sdesc(b0 + kk * (32 / C::kElem) * C::kAtomBytes, C::kAtomBlock);
           if constexpr (kFp8)
             mma_ts_f8(d, a + kk * 8, bd, C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
           else
@@ -763,7 +774,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const 
                           const fa_row_stats* stats, void* stream) {
   using namespace fa;
   clear_error();
-  if (d != 128) return set_error(FA_ERR_UNSUPPORTED, "the FP8 forward supports d=128 only (got %d)", d);
+  if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
   if (!descale) return set_error(FA_ERR_INVALID_ARG, "descale is NULL");
   if (reinterpret_cast<uintptr_t>(descale) & 3) return set_error(FA_ERR_INVALID_ARG, "descale is not 4-byte aligned");
   fwd::Params p;
@@ -776,5 +787,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const 
       (rc = make_tmap_u8_bhnd(&tk, k8, B * H, N, d, fwd::kBlockN)) ||
       (rc = make_tmap_u8_bhnd(&tv, v8, B * H, N, d, fwd::kBlockN)))
     return rc;
-  return dispatch_fwd<128, true>(stable, want_stats, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return d == 64 ? dispatch_fwd<64, true>(stable, want_stats, tq, tk, tv, p, s)
+                 : dispatch_fwd<128, true>(stable, want_stats, tq, tk, tv, p, s);
 }

@@ -25,8 +25,9 @@ uint32_t* device_status_word();
 // 128-byte swizzle and a (64 x box_rows x 1) box; out-of-range rows read as zero.
 int make_tmap_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
 
-// The same for a 1-byte (E4M3) tensor: a (128 x box_rows x 1) box, one 128-byte row per
-// box row when d = 128.
+// The same for a 1-byte (E4M3) tensor: one swizzle atom per box row -- a (128 x box_rows x 1)
+// box with a 128-byte swizzle for d = 128, a (64 x box_rows x 1) box with a 64-byte swizzle
+// for d = 64.
 int make_tmap_u8_bhnd(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
 
 // Encode a 3-D FP32 tensor map over a contiguous [BH, N, d] tensor with a 128-byte swizzle

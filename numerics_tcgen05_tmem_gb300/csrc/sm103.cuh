@@ -256,6 +256,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same for a 64-byte swizzle (layout 4): rows of 64 B in 8-row atoms of 512 B, used
+// when a tile row is 64 bytes (E4M3 with d = 64).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)4u << 61;
+  return d;
+}
+
 // ----------------------------------------------------------------- TMEM <-> registers
 // 32x32b shape: warp (w % 4) reaches lanes 32*(w%4) .. +31; thread t gets lane base+t,
 // .xN gives N consecutive 32-bit columns.

@@ -91,8 +91,8 @@ def test_fp8_invalid_arguments(lib):
     def fwd8(q=good, descale=ds, d=128, N=128, stable=1):
         return lib.fa_fwd_fp8(q, good, good, descale, good, good, 1, 1, N, d, 1, 0.125, stable, 1.25, None, None)
 
-    assert fwd8(d=64) == binding.FA_ERR_UNSUPPORTED
-    assert b"d=128" in lib.fa_last_error()
+    assert fwd8(d=96) == binding.FA_ERR_UNSUPPORTED
+    assert b"d=96" in lib.fa_last_error()
     assert fwd8(descale=None) == binding.FA_ERR_INVALID_ARG
     assert fwd8(descale=ctypes.c_void_p((1 << 21) + 2)) == binding.FA_ERR_INVALID_ARG
     assert fwd8(q=None) == binding.FA_ERR_INVALID_ARG

@@ -92,11 +92,12 @@ def test_quantize_full_size_tensors():
 
 # ----------------------------------------------------------------- forward
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("stable", [0, 1, 2])
-def test_tiny_ties_exact_statistics(stable):
+def test_tiny_ties_exact_statistics(stable, d):
     # k/8 with |k| <= 16 is exact in E4M3 and the dot products are exact in FP32, so with
     # unit scales the row maximum, ties, branch and the exact-1.0 counts are decidable
-    w = inputs.tiny_ties(d=128, N=300, H=2)
+    w = inputs.tiny_ties(d=d, N=300, H=2)
     vals = [t.double().numpy() for t in (w.q, w.k, w.v)]
     codes = [F.encode_e4m3(x) for x in vals]
     assert all(np.array_equal(F.decode_e4m3(c), x) for c, x in zip(codes, vals))
@@ -117,9 +118,10 @@ def test_tiny_ties_exact_statistics(stable):
 
 
 @pytest.mark.parametrize("N", [1, 100, 128, 129, 300, 1000])
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [True, False])
-def test_ragged_shapes(N, causal):
-    w = inputs.random_case(2, 2, N, 128, causal, seed=N * 13 + 5, std=1.5)
+def test_ragged_shapes(N, d, causal):
+    w = inputs.random_case(2, 2, N, d, causal, seed=N * 13 + d + 5, std=1.5)
     codes, ds = oracle_quantized(w)
     o, lse = run_fp8(codes, ds, w, 1, stats=False)
     deq = dequantized(codes, ds)
@@ -196,3 +198,13 @@ def test_extreme_16k_noncausal_sampled_head():
     ref = F.forward_fp8(*sub, ds, w.scale, False, stable=1, beta=w.beta)
     assert rel_fro(o[:, [7]], ref["o"]) <= FP8_REL_TOL
     assert_lse(lse[:, [7]], ref["lse"])
+
+
+def test_gpt2_small_full():
+    # the d = 64 workload in full: E4M3 rows of 64 bytes (64-byte swizzle) and the S ring
+    w = inputs.gpt2_small()
+    codes, ds = oracle_quantized(w)
+    o, lse = run_fp8(codes, ds, w, 1, stats=False)
+    ref = F.forward_fp8(*codes, ds, w.scale, True, stable=1, beta=w.beta)
+    assert rel_fro(o, ref["o"]) <= FP8_REL_TOL
+    assert_lse(lse, ref["lse"])
