@@ -60,11 +60,12 @@ struct Cfg {
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
   static constexpr int kDSOff = kDOOff + kTileBytes;                // dS^T, 128 x 128 BF16
-  // dQ staging: half a dQ tile (128 rows x D/2 FP32 columns) as 128B-swizzled boxes of
-  // 32 columns x 128 rows, the source of the TMA reduce-add into the accumulator
-  static constexpr int kDQBoxes = D / 64;
+  // dQ staging: a ring of four 128B-swizzled slots of 32 FP32 columns x 64 rows (8 KB), the
+  // sources of the TMA reduce-adds into the accumulator; a 32-column group of a dQ tile
+  // takes two slots (rows 0-63, 64-127)
+  static constexpr int kDQSlot = 64 * 128;
   static constexpr int kDQOff = kDSOff + kBlock * kBlock * 2;
-  static constexpr int kLseOff = kDQOff + kDQBoxes * 16384;          // lse*log2(e), per stage
+  static constexpr int kLseOff = kDQOff + 4 * kDQSlot;               // lse*log2(e), per stage
   static constexpr int kDeltaOff = kLseOff + kStages * kBlock * 4;   // delta, per stage
   static constexpr int kBarOff = kDeltaOff + kStages * kBlock * 4;
   static constexpr int kSmemBytes = kBarOff + 256;
@@ -502,16 +503,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ dQ warpgroup
     // Each dQ tile leaves TMEM in one round trip (the whole row of D FP32 columns into
     // registers), so the columns go back to the MMA warp -- whose next dP^T product writes
-    // them -- as early as possible.  Then the tile is written in two halves, one row per
-    // thread, into the 128B-swizzled staging boxes and pushed into the FP32 accumulator by
-    // TMA reduce-adds issued by one thread (rows past N are dropped by the hardware).
+    // them -- as early as possible.  The tile is then pushed into the FP32 accumulator one
+    // 32-column group at a time: each group is written, one row per thread, into two
+    // 128B-swizzled slots of a four-slot ring and handed to TMA reduce-adds issued by one
+    // thread (rows past N are dropped by the hardware).  A group waits only for the group
+    // two before it to have been read, so the TMA engine always has work while the next
+    // group is written.
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegDQ));
     const int lane_base = (warp % 4) * 32;
     const int r = lane_base + (threadIdx.x % 32);  // query row within the current query tile
     const bool leader = (r == 0);
     const uint32_t tDQ = tmem + C::kTmemDQ + ((uint32_t)lane_base << 16);
-    uint8_t* stage_row = smem + C::kDQOff + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
+    int g_total = 0;  // 32-column groups pushed so far (slot pair = g_total % 2)
     for (int it = 0; it < n_it; ++it) {
       if (!mbar_wait(&sh.dq_full, it & 1, abort_flag, p.status)) break;
       tc_fence_after();
@@ -524,24 +528,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&sh.dq_empty);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        // the staging boxes are free once the previous reductions have read them
-        if (leader) bulk_wait_read_all();
+      for (int g = 0; g < D / 32; ++g, ++g_total) {
+        const int pair = g_total & 1;  // slots 2*pair (rows 0-63) and 2*pair + 1 (rows 64-127)
+        // the pair's previous group (two groups back) has been read
+        if (leader) bulk_wait_read_but_one();
         named_barrier(1, kBlock);
+        uint8_t* row = smem + C::kDQOff + (2 * pair + (r >> 6)) * C::kDQSlot + (r & 63) * 128;
 #pragma unroll
-        for (int b = 0; b < C::kDQBoxes; ++b)
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            const int c = half * (D / 2) + b * 32 + ch * 4;
-            *reinterpret_cast<uint4*>(stage_row + b * 16384 + (((uint32_t)ch ^ sw) << 4)) =
-                make_uint4(w[c], w[c + 1], w[c + 2], w[c + 3]);
-          }
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(row + (((uint32_t)ch ^ sw) << 4)) =
+              make_uint4(w[g * 32 + ch * 4], w[g * 32 + ch * 4 + 1], w[g * 32 + ch * 4 + 2], w[g * 32 + ch * 4 + 3]);
         fence_proxy_async_smem();
         named_barrier(1, kBlock);
         if (leader) {
-#pragma unroll
-          for (int b = 0; b < C::kDQBoxes; ++b)
-            tma_reduce_add_3d(&tmDQ, smem + C::kDQOff + b * 16384, half * (D / 2) + b * 32, q0, bh);
+          tma_reduce_add_3d(&tmDQ, smem + C::kDQOff + (2 * pair) * C::kDQSlot, g * 32, q0, bh);
+          tma_reduce_add_3d(&tmDQ, smem + C::kDQOff + (2 * pair + 1) * C::kDQSlot, g * 32, q0 + 64, bh);
           bulk_commit_group();
         }
       }
@@ -614,7 +615,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   CUtensorMap tdq;
   if ((rc = make_tmap_bhnd(&tq, q, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tk, k, B * H, N, D, bwd::kBlock)) ||
       (rc = make_tmap_bhnd(&tv, v, B * H, N, D, bwd::kBlock)) || (rc = make_tmap_bhnd(&tdo, dO, B * H, N, D, bwd::kBlock)) ||
-      (rc = make_tmap_f32_bhnd(&tdq, sc.dq_acc, B * H, N, D, bwd::kBlock)))
+      (rc = make_tmap_f32_bhnd(&tdq, sc.dq_acc, B * H, N, D, 64)))
     return rc;
   bwd::Params p{};
   p.lse2 = sc.lse2;
