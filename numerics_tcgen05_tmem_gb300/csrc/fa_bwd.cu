@@ -314,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                  C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
       };
       // Issue order (same-thread MMAs execute in order):
-      //   S_0 dP_0 dV_0 S_1 | dK_0 dQ_0 dV_1 dP_1 S_2 | dK_1 dQ_1 dV_2 dP_2 S_3 | ...
-      // so dK_i/dQ_i run while the softmax warpgroups compute P_{i+1}, and dV_{i+1} runs
-      // while dQ_i is drained from the columns dP_{i+1} needs.
+      //   S_0 dP_0 dV_0 S_1 | dK_0 dQ_0 dP_1 dV_1 S_2 | dK_1 dQ_1 dP_2 dV_2 S_3 | ...
+      // dP_{i+1} needs only dO and the drained dQ_i columns, so it runs while the softmax
+      // warpgroups compute P_{i+1}; dV_{i+1} follows once P_{i+1} is in TMEM.
       if (ok && n_it > 0) {
         tc_fence_after();
         issue_s(0);
@@ -345,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&sh.ds_empty);
         tc_commit(&sh.dq_full);
         if (it + 1 < n_it) {
-          issue_dv(it + 1);
-          if (!ok) break;
           issue_dp(it + 1);
+          if (!ok) break;
+          issue_dv(it + 1);
           if (!ok) break;
           tc_commit(&sh.do_empty);
           if (it + 2 < n_it) {
