@@ -27,8 +27,10 @@
 // 128-column row of S, the others need few.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1; the BF16 P~ of a tile is written
 // over the first 64 columns of its S (32 for E4M3; each thread has read its own S row
-// first) and fed to the P~V MMA straight from TMEM.  The row's block maximum comes with
-// the TMEM load of S (tcgen05.ld.red.max) whenever the block has no masked column.
+// first) and fed to the P~V MMA straight from TMEM.  At d = 128 P~ goes to TMEM in two
+// halves, and the MMA warp starts the first half's P~V while the second is computed.
+// The row's block maximum comes with the TMEM load of S (tcgen05.ld.red.max) whenever
+// the block has no masked column.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdio.h>
@@ -129,7 +131,8 @@ struct Shared {
   // per tile: event e lands on [e & 1] and is awaited with parity (e >> 1) & 1, so neither
   // barrier runs more than one phase ahead.  Without the ring only [0] is used, with
   // parity e & 1.  Events: S and P~ of block j (e = j); alpha and the corrected O of
-  // block j >= 1 (e = j - 1).
+  // block j >= 1 (e = j - 1).  Without the ring p_ready[t][1] carries the first half of
+  // P~ (keys 0-63 of the block), handed over before the second half is computed.
   uint64_t s_full[kTiles][2], p_ready[kTiles][2], pv_done[kTiles];
   uint64_t alpha_ready[kTiles][2], o_ready[kTiles][2], l_ready[kTiles];
   uint64_t mma_done;
@@ -278,12 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_t += P~_t V_j: P~ from TMEM (K = 128 keys, 8 columns = 32 bytes per k-step), V MN-major
       // (a k-step covers 32 / kElem keys of 128-byte rows)
-      auto issue_pv = [&](int t, int s, int j) {
+      auto issue_pv = [&](int t, int s, int j, int k_lo = 0, int k_hi = C::kKStepsO) {
         const uint32_t b0 = sV + s * C::kTileBytes;
         const uint32_t d = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1);
         const uint32_t a = tmem + C::s_col(t, j);
 #pragma unroll
-        for (int kk = 0; kk < C::kKStepsO; ++kk) {
+        for (int kk = k_lo; kk < k_hi; ++kk) {
           // a k-step covers 32 / kElem keys, one atom row (kAtomBytes) each; LBO = the next
           // atom column block along d (only with two or more)
           const uint64_t bd = C::sdesc(b0 + kk * (32 / C::kElem) * C::kAtomBytes, C::kAtomBlock);
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             mma_ts(d, a + kk * 8, bd, C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&sh.pv_done[t]);
+        if (k_hi == C::kKStepsO) tc_commit(&sh.pv_done[t]);
       };
       if constexpr (C::kRing) {
         // Order: S0_0 S1_0 S0_1 | PV0_0 S1_1 PV1_0 S0_2 | PV0_1 S1_2 PV1_1 S0_3 | ...
@@ -345,6 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // Order: S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 PV1_1 S1_2 | ... | PV0_last PV1_last
+        // Each P~V runs in two halves over the keys, the first as soon as the softmax has
+        // stored the first half of P~ (2-3 % faster than waiting for all of it; four or
+        // eight parts measured slower: the single issuer then waits on one tile too often).
         for (int j = 0; ok && j <= nbmax; ++j) {
           const int s = j % C::kStages;
           const uint32_t ph = (j / C::kStages) & 1;
@@ -359,12 +365,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int t = 0; t < kTiles; ++t) {
             if (j > 0 && j - 1 < nb[t]) {
-              if (!(ok = mbar_wait(&sh.p_ready[t][0], ev_parity<false>(j - 1), abort_flag, p.status))) break;
+              // the first half of P~ (keys 0-63) is handed over before the second is computed
+              if (!(ok = mbar_wait(&sh.p_ready[t][1], ev_parity<false>(j - 1), abort_flag, p.status))) break;
               // O_t must carry block j-1's correction (applied by the correction warpgroup)
               if (j - 1 > 0 && !(ok = mbar_wait(&sh.o_ready[t][0], ev_parity<false>(j - 2), abort_flag, p.status)))
                 break;
               tc_fence_after();
-              issue_pv(t, sp, j - 1);
+              issue_pv(t, sp, j - 1, 0, C::kKStepsO / 2);
+              if (!(ok = mbar_wait(&sh.p_ready[t][0], ev_parity<false>(j - 1), abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_pv(t, sp, j - 1, C::kKStepsO / 2, C::kKStepsO);
             }
             if (j < nb[t]) issue_s(t, s, j);
           }
@@ -505,14 +515,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kFp8) {
         uint32_t pk[kBlockN / 4];
 #pragma unroll
-        for (int i = 0; i < kBlockN; i += 4) {
-          float x0, x1, x2, x3;
-          fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);       // scale*log2(e)*dq*dk * (S - m) + 8
-          fma2(x2, x3, sv[i + 2], sv[i + 3], c, c, nmc, nmc);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          add2(sum0, sum1, sum0, sum1, p0, p1);
-          add2(sum0, sum1, sum0, sum1, p2, p3);
-          pk[i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = h * 64; i < h * 64 + 64; i += 4) {
+            float x0, x1, x2, x3;
+            fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);       // scale*log2(e)*dq*dk * (S - m) + 8
+            fma2(x2, x3, sv[i + 2], sv[i + 3], c, c, nmc, nmc);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            add2(sum0, sum1, sum0, sum1, p0, p1);
+            add2(sum0, sum1, sum0, sum1, p2, p3);
+            pk[i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+          if constexpr (!C::kRing) {
+            __syncwarp();
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pk[h * 16 + i];
+            tmem_st16(tS + h * 16, w);
+            if (h == 0) {
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(&sh.p_ready[t][1]);
+            }
+          }
         }
         if constexpr (kStats) {
           // an entry of exactly 1.0 is 2^8 = E4M3 code 0x78 after the scaling
@@ -521,31 +546,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int b = 0; b < 4; ++b) ones += (((pk[i] >> (8 * b)) & 0xFFu) == 0x78u) ? 1 : 0;
         }
-        __syncwarp();
-        tmem_st32(tS, pk);
+        if constexpr (C::kRing) {
+          __syncwarp();
+          tmem_st32(tS, pk);
+        }
       } else {
         uint32_t pk[kBlockN / 2];
 #pragma unroll
-        for (int i = 0; i < kBlockN; i += 2) {
-          float x0, x1;
-          fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);   // scale*log2(e) * (S - m)
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          add2(sum0, sum1, sum0, sum1, p0, p1);
-          pk[i / 2] = pack_bf16x2(p0, p1);
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int i = h * 64; i < h * 64 + 64; i += 2) {
+            float x0, x1;
+            fma2(x0, x1, sv[i], sv[i + 1], c, c, nmc, nmc);   // scale*log2(e) * (S - m)
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            add2(sum0, sum1, sum0, sum1, p0, p1);
+            pk[i / 2] = pack_bf16x2(p0, p1);
+          }
+          __syncwarp();
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = pk[h * 32 + i];
+          tmem_st32(tS + h * 32, w);
+          if constexpr (!C::kRing) {
+            if (h == 0) {
+              tmem_st_wait();
+              tc_fence_before();
+              mbar_arrive(&sh.p_ready[t][1]);
+            }
+          }
         }
         if constexpr (kStats) {
 #pragma unroll
           for (int i = 0; i < kBlockN / 2; ++i)
             ones += ((pk[i] & 0xFFFFu) == 0x3F80u ? 1 : 0) + ((pk[i] >> 16) == 0x3F80u ? 1 : 0);
-        }
-        __syncwarp();
-        uint32_t w[32];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = pk[h * 32 + i];
-          tmem_st32(tS + h * 32, w);
         }
       }
       {
