@@ -134,10 +134,17 @@ struct Shared {
   // block j >= 1 (e = j - 1).  Without the ring p_ready[t][1] carries the first half of
   // P~ (keys 0-63 of the block), handed over before the second half is computed.
   uint64_t s_full[kTiles][2], p_ready[kTiles][2], pv_done[kTiles];
+  // o_done[t]: the last P~V of tile t has completed (committed once, after it).  The epilogue
+  // waits on it rather than on pv_done's parity, which could alias if it ran two products
+  // behind.
+  uint64_t o_done[kTiles];
   uint64_t alpha_ready[kTiles][2], o_ready[kTiles][2], l_ready[kTiles];
   uint64_t mma_done;
   uint64_t never;  // test builds only: a barrier nothing arrives on
-  float alpha[kTiles][kBlockM];  // correction factor of each row for the current block
+  // correction factor of each row, by alpha event parity: a softmax can hand over the next
+  // block's factor before the correction warpgroup has read the current one only with the
+  // d = 64 ring, and never two ahead (the P~V that gates its next S waits for that read)
+  float alpha[kTiles][2][kBlockM];
   float lfin[kTiles][kBlockM];   // final row sums for the epilogue
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -189,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.p_ready[t][0], kBlockM);
       mbar_init(&sh.p_ready[t][1], kBlockM);
       mbar_init(&sh.pv_done[t], 1);
+      mbar_init(&sh.o_done[t], 1);
       mbar_init(&sh.alpha_ready[t][0], kBlockM);
       mbar_init(&sh.alpha_ready[t][1], kBlockM);
       mbar_init(&sh.o_ready[t][0], kBlockM);
@@ -295,7 +303,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             mma_ts(d, a + kk * 8, bd, C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        if (k_hi == C::kKStepsO) tc_commit(&sh.pv_done[t]);
+        if (k_hi == C::kKStepsO) {
+          tc_commit(&sh.pv_done[t]);
+          if (j == nb[t] - 1) tc_commit(&sh.o_done[t]);
+        }
       };
       if constexpr (C::kRing) {
         // Order: S0_0 S1_0 S0_1 | PV0_0 S1_1 PV1_0 S0_2 | PV0_1 S1_2 PV1_1 S0_3 | ...
@@ -506,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = ex2_approx((m - m_new) * c);  // 0 on the first block (m = -inf)
       if (j > 0) {
         // hand the row's correction factor to the correction warpgroup right away
-        sh.alpha[t][r] = alpha;
+        sh.alpha[t][(j - 1) & 1][r] = alpha;
         mbar_arrive(&sh.alpha_ready[t][ev_slot<C::kRing>(j - 1)]);
       }
       // FP8: P~ * 2^8 (added to the exponent) uses the E4M3 range below 448 instead of <= 1
@@ -634,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(&sh.alpha_ready[t][ev_slot<C::kRing>(j - 1)], ev_parity<C::kRing>(j - 1), abort_flag,
                              p.status)))
           break;
-        const float alpha = sh.alpha[t][r];
+        const float alpha = sh.alpha[t][(j - 1) & 1][r];
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           // the previous P~V of this tile has landed (its S_j commit already implies it)
           if (!(ok = mbar_wait(&sh.pv_done[t], (j - 1) & 1, abort_flag, p.status))) break;
@@ -664,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue: O = O / l -> BF16
     for (int t = 0; ok && t < kTiles; ++t) {
       if (nb[t] == 0) continue;
-      if (!(ok = mbar_wait(&sh.pv_done[t], (nb[t] - 1) & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.o_done[t], 0, abort_flag, p.status))) break;
       if (!(ok = mbar_wait(&sh.l_ready[t], 0, abort_flag, p.status))) break;
       tc_fence_after();
       // FP8: O = (P~ 2^8)_E4M3 V8 * dv / (l 2^8); the 2^8 is in both sums
