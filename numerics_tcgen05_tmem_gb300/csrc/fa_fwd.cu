@@ -452,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // block max: from the loads' reductions when no row of the warp has a masked column,
       // else over the masked values with 3-input max in four independent chains
       float bm;
-      if (__all_sync(0xffffffffu, lim >= kBlockN)) {
+      const bool unmasked = __all_sync(0xffffffffu, lim >= kBlockN);
+      if (unmasked) {
         bm = fmaxf(max3f(pmax[0], pmax[1], pmax[2]), pmax[3]);
       } else {
         float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
@@ -483,7 +484,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // running (max, count) merge: rs' = [rm == rm'] rs + [bm == rm'] bc.  The block's
         // count only matters when bm reaches the running max (or, block-locally, always),
         // so a warp whose rows all have bm < rm skips counting.
-        if (kStable == 2 || __any_sync(0xffffffffu, bm >= rm)) {
+        if (kStable != 2 && unmasked) {
+          // Only a 32-column chunk whose load-time maximum equals the block maximum can hold
+          // it, and only rows with bm >= rm need the count: the warp counts just the chunks
+          // one of those rows needs (exact -- a skipped chunk has no entry equal to bm in
+          // any row that uses bc).
+          const bool need = bm >= rm;
+          uint32_t neg0 = 0, neg1 = 0;
+#pragma unroll
+          for (int c0 = 0; c0 < kBlockN / 32; ++c0) {
+            if (__any_sync(0xffffffffu, need && pmax[c0] == bm)) {
+#pragma unroll
+              for (int i = c0 * 32; i < c0 * 32 + 32; i += 4) {
+                neg0 += eq_mask(sv[i], bm) + eq_mask(sv[i + 1], bm);
+                neg1 += eq_mask(sv[i + 2], bm) + eq_mask(sv[i + 3], bm);
+              }
+            }
+          }
+          bc = (bm == -INFINITY) ? 0 : -(int)(neg0 + neg1);
+        } else if (kStable == 2 || __any_sync(0xffffffffu, bm >= rm)) {
           // each equality gives an all-ones mask (-1); two masks per three-input add
           uint32_t neg0 = 0, neg1 = 0;
 #pragma unroll
