@@ -135,8 +135,10 @@ int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* desc
 
 /*
  * fa_bwd_workspace_size -- bytes of device scratch fa_bwd needs: an FP32
- * [B,H,N,d] dQ accumulator plus an FP32 [B,H,N] delta, each rounded up to
- * 256 bytes.  Returns 0 for invalid sizes.
+ * [B,H,N,d] dQ accumulator, then lse*log2(e) and delta as FP32 [B,H,N_pad]
+ * (N_pad = N rounded up to a multiple of 128; the padding holds lse = +inf
+ * and delta = 0), each part rounded up to 256 bytes.  Returns 0 for invalid
+ * sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
