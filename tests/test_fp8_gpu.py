@@ -92,12 +92,14 @@ def test_quantize_full_size_tensors():
 
 # ----------------------------------------------------------------- forward
 
+@pytest.mark.parametrize("N", [300, 2048])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("stable", [0, 1, 2])
-def test_tiny_ties_exact_statistics(stable, d):
+def test_tiny_ties_exact_statistics(stable, d, N):
     # k/8 with |k| <= 16 is exact in E4M3 and the dot products are exact in FP32, so with
     # unit scales the row maximum, ties, branch and the exact-1.0 counts are decidable
-    w = inputs.tiny_ties(d=d, N=300, H=2)
+    # (N = 2048: 16 key blocks, with ties first reached late in the row)
+    w = inputs.tiny_ties(d=d, N=N, H=2)
     vals = [t.double().numpy() for t in (w.q, w.k, w.v)]
     codes = [F.encode_e4m3(x) for x in vals]
     assert all(np.array_equal(F.decode_e4m3(c), x) for c, x in zip(codes, vals))

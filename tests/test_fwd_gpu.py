@@ -45,6 +45,32 @@ def test_tiny_ties_bit_exact_stats(stable):
         assert np.all(st["row_ones"].cpu().numpy()[rep] >= ref["rs"][rep])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("stable", [0, 1])
+def test_long_dyadic_rows_exact_statistics(stable, causal, d):
+    # 16 key blocks of exact (dyadic) scores with copied key rows: a few hundred rows have a
+    # repeated maximum, many of them first reached late in the row.  There the kernel
+    # counts ties only in the 32-column chunks that can hold a row's new maximum; the raw
+    # maxima, tie counts and branches must still equal the oracle's exactly, and the
+    # exact-1.0 counts the BF16 emulation's.
+    w0 = inputs.tiny_ties(N=2048, H=2, d=d)
+    w = inputs.Workload(w0.name, w0.q, w0.k, w0.v, w0.do, causal, w0.scale, stable, w0.beta)
+    o, lse, st = run_fwd(w, stable)
+    ref = A.forward(w.q, w.k, w.v, w.scale, causal, stable=stable, beta=w.beta)
+    assert (ref["rs"] > 1).sum() > 100
+    assert_close_bf16("o", o, ref["o"])
+    assert_lse(lse, ref["lse"])
+    np.testing.assert_array_equal(st["row_max_raw"].cpu().numpy().astype(np.float64), ref["rm"])
+    np.testing.assert_array_equal(st["row_ties"].cpu().numpy(), ref["rs"])
+    np.testing.assert_array_equal(st["row_branch"].cpu().numpy(), ref["branch"])
+    em = E.blocked_forward(w.q, w.k, w.v, w.scale, causal, stable=stable, beta=w.beta, block_n=128)
+    np.testing.assert_array_equal(st["row_ones"].cpu().numpy(), em["ones"])
+    # the statistics-free kernel decides the same shifts: identical O and LSE
+    o2, lse2 = run_fwd(w, stable, stats=False)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
 @pytest.mark.parametrize("stable", [0, 1])
 def test_gpt2_small_full(stable):
     w = inputs.gpt2_small()
