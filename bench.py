@@ -10,11 +10,12 @@ peak.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
-Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle (numpy
-FP64) on the host cores instead, on a bounded sample of the same workload.
-Under torchrun with N > 1 every rank runs its own independent shard of
-(batch, head) problems of the same size (weak scaling, no collective on the
-data path); timing is the max over ranks.
+Prints one JSON line (rank 0); its "configs" block times forward (plain and
+stabilised), backward and FP8 forward of every workload after the timed steps.
+`--impl reference` times the CPU oracle (numpy FP64) on the host cores instead,
+on a bounded sample of the same workload.  Under torchrun with N > 1 every rank
+runs a replica of the same problem on its own GPU (weak scaling, no collective on
+the data path); timing is the max over ranks.
 """
 from __future__ import annotations
 
@@ -355,11 +356,17 @@ def run_native(args):
     link_h2d = link_gbs(dev_in[0][0], host[0])
     link_d2h = link_gbs(host_out[0][0], dev_out[0][0])
     binding.device_status(stream)
-    for a_, b_ in zip((o, dq, dk, dv), (host_out[(E - 1) % 2][0], host_out[(E - 1) % 2][2], host_out[(E - 1) % 2][3],
-                                         host_out[(E - 1) % 2][4])):
-        # the pipelined results are the same computation as the device-resident steps
-        if not torch.equal(a_[0, 0, :64].cpu(), b_[0, 0, :64]) and a_ is not dq:
-            raise RuntimeError("end-to-end results differ from the device-resident run")
+    # The pipelined steps compute what the device-resident steps did: the last one's results,
+    # as copied to the host, must equal O, LSE, dK and dV bit for bit; dQ sums FP32 reduce-adds
+    # in an order that may differ, so it must agree to 1e-3 relative Frobenius error.
+    last = host_out[(E - 1) % NBUF]
+    for name, a_, b_ in (("o", o, last[0]), ("lse", lse, last[1]), ("dk", dk, last[3]), ("dv", dv, last[4])):
+        if not torch.equal(a_.cpu(), b_):
+            raise RuntimeError(f"end-to-end {name} differs from the device-resident run")
+    dq_host = dq.cpu().float()
+    dq_err = float((last[2].float() - dq_host).norm() / dq_host.norm().clamp_min(1e-30))
+    if not dq_err <= 1e-3:
+        raise RuntimeError(f"end-to-end dq differs from the device-resident run ({dq_err:.2e})")
 
     # ---------------- FP8 forward (E4M3 with dynamic per-tensor scales) on the same workload,
     # after the timed BF16 steps: quantise Q, K, V on the GPU once, then time fa_fwd_fp8 alone
@@ -387,6 +394,13 @@ def run_native(args):
     binding.device_status(stream)
     fp8_ms = ev8[0].elapsed_time(ev8[1]) / R8
     quant_ms = evq[0].elapsed_time(evq[1]) / R8
+
+    # every workload, after the timed steps: forward plain and stabilised, backward, FP8 forward
+    configs = None
+    if not args.no_configs:
+        keep = ("workload", "what", "fwd_stable0_tflops", "fwd_stable0_frac", "fwd_stable1_tflops",
+                "fwd_stable1_frac", "bwd_tflops", "bwd_frac", "fp8_fwd_stable1_tflops", "l2_flush")
+        configs = [{k2: r[k2] for k2 in keep if k2 in r} for r in measure_configs()]
 
     peaks = load_peaks()
     peak = peaks["bf16_tflops"]
@@ -421,7 +435,8 @@ def run_native(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "steps": E, "pipelining": "copy-in, compute and copy-out streams, triple-buffered device buffers; the forward starts once Q, K, V are in, O and LSE go out while the backward runs",
                 "link_gbs": {"h2d": round(link_h2d, 1), "d2h": round(link_d2h, 1),
-                             "note": "one 67 MB pinned copy alone; bounds e2e at (h2d + d2h bytes) / bandwidth"}},
+                             "note": "one 67 MB pinned copy alone; bounds e2e at (h2d + d2h bytes) / bandwidth"},
+                "check": {"o_lse_dk_dv": "bit-identical to the device-resident step", "dq_rel_fro": dq_err}},
         "fp8_forward": {
             "kernel": "fa_fwd_kernel<128,stable,fp8>", "tflops": round(ff / (fp8_ms * 1e-3) / 1e12, 1),
             "ms": round(fp8_ms, 4), "launches_timed": R8,
@@ -433,6 +448,7 @@ def run_native(args):
             "quantize_bytes": "5 bytes per element: 2 read for amax, 2 read + 1 written for the codes"},
         "gpu_launches": 4 * K,
         "roofline": roofline,
+        "configs": configs,
         "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -466,25 +482,34 @@ def run_profile_case(args):
 
 
 # --------------------------------------------------------------------------- every workload
-def run_configs(args):
-    """Forward (plain and stabilised) and backward time of each workload: one JSON line each.
+CONFIG_CASES = (
+    ("tiny_ties", "tiny ties B=1 H=2 N=128 d=64 causal", lambda I: I.tiny_ties()),
+    ("gpt2_small", "GPT-2-small B=8 H=12 N=1024 d=64 causal", lambda I: I.gpt2_small()),
+    ("gpt2_medium_sink", "GPT-2-medium with sink B=16 H=16 N=1024 d=64 causal", lambda I: I.gpt2_medium_sink()),
+    ("llama7b_long", "LLaMA-7B shaped B=1 H=32 N=8192 d=128 causal", lambda I: I.llama7b_long()),
+    ("extreme_16k_causal", "extreme length B=1 H=16 N=16384 d=128 causal", lambda I: I.extreme_16k()),
+    ("extreme_16k_noncausal", "extreme length B=1 H=16 N=16384 d=128 non-causal",
+     lambda I: I.extreme_16k(causal=False)),
+)
 
-    CUDA events after 3 warm-ups: inputs larger than the L2 are timed over R launches back to
-    back; the GPT-2-sized inputs fit in L2, so each of their R launches is timed alone after a
-    256 MB buffer is rewritten to flush it.
+
+def measure_configs(with_fp8=True, R=10):
+    """Forward (plain and stabilised), backward (and FP8 forward) time of every workload.
+
+    CUDA events after 3 warm-ups on the current stream: inputs larger than the L2 are timed
+    over R launches back to back; the GPT-2-sized inputs fit in L2, so each of their R
+    launches is timed alone after a 256 MB buffer is rewritten to flush it.  Returns one
+    dict per workload with TFLOP/s and the fraction of the measured dense BF16 peak.
     """
     import torch
 
-    from numerics_tcgen05_tmem_gb300 import binding, build, inputs
+    from numerics_tcgen05_tmem_gb300 import binding, inputs
 
-    build.build()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     peak = load_peaks()["bf16_tflops"]
-    cases = [("tiny_ties", inputs.tiny_ties()), ("gpt2_small", inputs.gpt2_small()),
-             ("gpt2_medium_sink", inputs.gpt2_medium_sink()), ("llama7b_long", inputs.llama7b_long()),
-             ("extreme_16k_causal", inputs.extreme_16k()), ("extreme_16k_noncausal", inputs.extreme_16k(causal=False))]
-    R = 10
-    for name, w in cases:
+    rows = []
+    for name, label, make in CONFIG_CASES:
+        w = make(inputs)
         q, k, v, do = (t.to("cuda") for t in (w.q, w.k, w.v, w.do))
         B, H, N, d = q.shape
         small = q.numel() * 2 * 4 < 129e6
@@ -495,7 +520,6 @@ def run_configs(args):
                 fn()
             torch.cuda.synchronize()
             if not small:
-                # inputs larger than L2: R launches back to back, as in the step timing
                 e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
                 e[0].record()
                 for _ in range(R):
@@ -515,32 +539,91 @@ def run_configs(args):
             return tot / R
 
         ff = flops_fwd(B, H, N, d, w.causal)
-        line = {"workload": name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal, "scale": w.scale,
-                "l2_flush": small}
+        line = {"workload": name, "what": label, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                "scale": w.scale, "l2_flush": small}
         for stable in (0, 1):
             ms = timed(lambda: binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=stable, beta=w.beta))
             line[f"fwd_stable{stable}_ms"] = round(ms, 4)
             line[f"fwd_stable{stable}_tflops"] = round(ff / (ms * 1e-3) / 1e12, 1)
+            line[f"fwd_stable{stable}_frac"] = round(ff / (ms * 1e-3) / 1e12 / peak, 4)
         o, lse = binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=1, beta=w.beta)
         ms = timed(lambda: binding.backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, workspace=ws))
-        # FP8 forward on the same inputs (quantised once on the GPU)
-        (q8, dq8), (k8, dk8), (v8, dv8) = (binding.quantize_fp8(t) for t in (q, k, v))
-        desc = torch.cat([dq8, dk8, dv8])
-        ms8 = timed(lambda: binding.forward_fp8(q8, k8, v8, desc, causal=w.causal, scale=w.scale, stable=1,
-                                                beta=w.beta))
-        line["fp8_fwd_stable1_ms"] = round(ms8, 4)
-        line["fp8_fwd_stable1_tflops"] = round(ff / (ms8 * 1e-3) / 1e12, 1)
-        del q8, k8, v8
         line["bwd_ms"] = round(ms, 4)
         line["bwd_tflops"] = round(2.5 * ff / (ms * 1e-3) / 1e12, 1)
-        line["fwd_stable1_frac_of_peak"] = round(line["fwd_stable1_tflops"] / peak, 4)
-        line["bwd_frac_of_peak"] = round(line["bwd_tflops"] / peak, 4)
+        line["bwd_frac"] = round(2.5 * ff / (ms * 1e-3) / 1e12 / peak, 4)
         # HBM view of the forward: Q, K, V read and O written once, plus the LSE
-        line["fwd_stable1_hbm_gbs"] = round((4 * q.numel() * 2 + B * H * N * 4) / (line["fwd_stable1_ms"] * 1e-3) / 1e9, 1)
+        line["fwd_stable1_hbm_gbs"] = round((4 * q.numel() * 2 + B * H * N * 4) / (line["fwd_stable1_ms"] * 1e-3) / 1e9,
+                                            1)
+        if with_fp8:
+            (q8, dq8), (k8, dk8), (v8, dv8) = (binding.quantize_fp8(t) for t in (q, k, v))
+            desc = torch.cat([dq8, dk8, dv8])
+            ms8 = timed(lambda: binding.forward_fp8(q8, k8, v8, desc, causal=w.causal, scale=w.scale, stable=1,
+                                                    beta=w.beta))
+            line["fp8_fwd_stable1_ms"] = round(ms8, 4)
+            line["fp8_fwd_stable1_tflops"] = round(ff / (ms8 * 1e-3) / 1e12, 1)
+            del q8, k8, v8
         binding.device_status()
-        print(json.dumps(line), flush=True)
+        rows.append(line)
         del q, k, v, do, o, lse, ws
         torch.cuda.empty_cache()
+    return rows
+
+
+def oracle_config_time(name, heads=None):
+    """Seconds and GFLOP of one oracle forward + backward of a workload (or `heads` of it)."""
+    from numerics_tcgen05_tmem_gb300 import inputs
+    from oracle import attention as A
+    make = {n: m for n, _, m in CONFIG_CASES}[name]
+    w = make(inputs)
+    h_full = w.q.shape[1]
+    if heads is not None:
+        sel = list(range(heads))
+        w = inputs.Workload(w.name, w.q[:, sel], w.k[:, sel], w.v[:, sel], w.do[:, sel], w.causal, w.scale, w.stable,
+                            w.beta)
+    B, H, N, d = w.q.shape
+    t0 = time.perf_counter()
+    f = A.forward(w.q, w.k, w.v, w.scale, w.causal, stable=1, beta=w.beta)
+    A.backward(w.q, w.k, w.v, f["o"], f["lse"], w.do, w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    return dt, (flops_fwd(B, H, N, d, w.causal) + flops_bwd(B, H, N, d, w.causal)) / 1e9, h_full
+
+
+def cpu_configs():
+    """The oracle (numpy FP64) on the host cores for every workload: the first three in full,
+    the long ones on 2 heads (time x H/2, labelled extrapolated), and the GPT-2-small workload
+    once more on a single thread (a child process with the BLAS thread pools set to 1)."""
+    out = []
+    for name, _, _ in CONFIG_CASES:
+        full = name in ("tiny_ties", "gpt2_small", "gpt2_medium_sink")
+        dt, gf, H = oracle_config_time(name, None if full else 2)
+        row = {"workload": name, "oracle_s": round(dt, 2), "oracle_gflops": round(gf / dt, 2), "cores": cpu_cores(),
+               "sample": "all heads"}
+        if not full:
+            row["oracle_s"] = round(dt * H / 2, 2)
+            row["sample"] = f"2 of {H} heads timed, extrapolated x {H // 2}"
+        out.append(row)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, bench; dt, gf, _ = bench.oracle_config_time('gpt2_small'); "
+            "print(json.dumps({'oracle_s': dt, 'gflop': gf}))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True)
+    if r.returncode == 0:
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        out.append({"workload": "gpt2_small", "oracle_s": round(one["oracle_s"], 2),
+                    "oracle_gflops": round(one["gflop"] / one["oracle_s"], 2), "cores": 1,
+                    "sample": "all heads, one thread"})
+    return out
+
+
+def run_configs(args):
+    """Every workload: GPU times (one JSON line each), then the oracle on the host cores."""
+    from numerics_tcgen05_tmem_gb300 import build
+
+    build.build()
+    for line in measure_configs():
+        print(json.dumps(line), flush=True)
+    if not args.no_cpu_baseline:
+        for line in cpu_configs():
+            print(json.dumps({"cpu_oracle": line}), flush=True)
 
 
 # --------------------------------------------------------------------------- reference arm (the oracle)
@@ -581,6 +664,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("native", "reference"), default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload block of the bench line")
     ap.add_argument("--configs", action="store_true",
                     help="time forward and backward of every workload (one JSON line each) and exit")
     ap.add_argument("--profile-case", action="store_true",

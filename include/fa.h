@@ -18,7 +18,8 @@
  *            running max / log-sum-exp bookkeeping.
  *   [cnnet]  "FlashAttention 训练时为什么会梯度爆炸？" §2: the backward recomputes
  *            the forward's probabilities from Q, K, V instead of storing them;
- *            §3.1 Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V.
+ *            §3.1 Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V; §3.3 an
+ *            overflow check on the backward's gradients.
  *   [web578] "為什么BF16的FlashAttention會把訓練「炸掉」？" mechanism 2: detect a
  *            repeated row maximum and shift so the exponent at the maximum is
  *            strictly below 1.
@@ -34,10 +35,13 @@
  *   - lse is the natural-log logsumexp of the scaled logits scale*q.k.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream).  The return value reports argument and launch errors
- *     only; errors raised on the device (a bounded wait that timed out) are
- *     read with fa_device_status().
- *   - The library allocates nothing per call.  It keeps one 4-byte status
- *     word per device, allocated on first use.
+ *     only; errors raised on the device (a bounded wait that timed out, a
+ *     non-finite output) are read with fa_device_status() or
+ *     fa_device_report_read().
+ *   - The library allocates nothing per call.  It keeps one 64-byte status
+ *     record per device (fa_device_report), allocated on first use.
+ *     fa_bwd_noalloc uses a separate, static record of its own, read with
+ *     fa_bwd_noalloc_status().
  */
 #ifndef FA_H_
 #define FA_H_
@@ -55,9 +59,33 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d not in {64, 128}) */
   FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed; see fa_last_error() */
   FA_ERR_TIMEOUT = 4,       /* (fa_device_status) a kernel's bounded wait ran out */
-  FA_ERR_DEVICE_BOUNDS = 5, /* (fa_device_status) a device-side layout check fired */
+  FA_ERR_DEVICE_BOUNDS = 5, /* (fa_device_status) a device-side index or layout check fired */
   FA_WARN_NONFINITE = 6     /* (fa_device_status) an output (O, LSE, dQ, dK or dV) held NaN or Inf */
 } fa_status;
+
+/* Which output a non-finite count of fa_device_report belongs to. */
+enum { FA_OUT_O = 0, FA_OUT_LSE = 1, FA_OUT_DQ = 2, FA_OUT_DK = 3, FA_OUT_DV = 4, FA_NUM_OUTPUTS = 5 };
+
+/* Bits of fa_device_report.flags. */
+enum { FA_DEVFLAG_TIMEOUT = 1, FA_DEVFLAG_BOUNDS = 2, FA_DEVFLAG_NONFINITE = 4 };
+
+/*
+ * What the kernels recorded on the device since the record was last read (the NaN monitor
+ * of [ijyty §7.1] and [jsqmd §5], per output; the overflow check in the backward that
+ * [cnnet §3.3] describes for CANN 8.0).
+ *   flags        : FA_DEVFLAG_* bits
+ *   bounds_site  : builds with FA_DEBUG_BOUNDS: the site id of the first failed index
+ *                  check (0 = none); bounds_value: the index that check saw
+ *   nonfinite[i] : how many entries of output i (FA_OUT_*) were written as NaN or Inf,
+ *                  counted on the stored values (BF16 for O, dQ, dK, dV; FP32 for LSE)
+ */
+typedef struct {
+  uint32_t flags;
+  uint32_t bounds_site;
+  int64_t bounds_value;
+  uint64_t nonfinite[FA_NUM_OUTPUTS];
+  uint64_t reserved;
+} fa_device_report;
 
 /* Shift branch codes written to fa_row_stats.row_branch. */
 enum { FA_BRANCH_RM = 0, FA_BRANCH_BETA = 1, FA_BRANCH_ZERO = 2 };
@@ -196,9 +224,11 @@ int fa_bwd_staged(const void* q, const void* k, const void* v, const void* o, co
  *     start at zero on each call; calls that overlap on the GPU (different streams,
  *     or host threads racing) race on the scratch and give wrong results: serialise
  *     them.
- *   - Device-side timeouts of this entry point are recorded in its own static
- *     status word, not the one fa_device_status() reads.
- * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA.
+ *   - What its kernels record on the device (a bounded wait that timed out, an index
+ *     check, non-finite gradients) goes to a static status record of its own, not the
+ *     one fa_device_status() reads: read it with fa_bwd_noalloc_status().
+ * Returns FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED or FA_ERR_CUDA (argument and
+ * launch errors; device-side errors come from fa_bwd_noalloc_status()).
  */
 #define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -207,14 +237,33 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    float scale, void* stream);
 
 /*
+ * fa_bwd_noalloc_status -- synchronise `stream`, then read and clear the status record
+ * that fa_bwd_noalloc's kernels write on the current device.  Allocates nothing (the
+ * record is a static device variable; its address was looked up by the first
+ * fa_bwd_noalloc call on the device, or is looked up here).  `out` may be NULL; when
+ * given, it receives the record as it was before clearing.
+ * Returns FA_OK, FA_ERR_TIMEOUT, FA_ERR_DEVICE_BOUNDS or FA_WARN_NONFINITE (in that
+ * order of precedence), or FA_ERR_CUDA if the synchronisation or the copy fails.
+ */
+int fa_bwd_noalloc_status(void* stream, fa_device_report* out);
+
+/*
  * fa_device_status -- synchronise `stream`, then return and clear the current
- * device's status word: FA_OK, FA_ERR_TIMEOUT, FA_ERR_DEVICE_BOUNDS or
+ * device's status record: FA_OK, FA_ERR_TIMEOUT, FA_ERR_DEVICE_BOUNDS or
  * FA_WARN_NONFINITE (in that order of precedence; FA_ERR_CUDA if the
  * synchronisation itself fails).  FA_WARN_NONFINITE is the NaN monitor of
  * [jsqmd §5] / [ijyty §7.1]: some output written since the last read held a
  * NaN or an Inf (e.g. from non-finite inputs); the call itself completed.
  */
 int fa_device_status(void* stream);
+
+/*
+ * fa_device_report_read -- the same as fa_device_status, and also copies the record
+ * (flags, first failed index check, non-finite count per output) into `out` (non-NULL)
+ * before it is cleared, so a caller can tell which output held NaN or Inf and how many
+ * entries did.
+ */
+int fa_device_report_read(void* stream, fa_device_report* out);
 
 /* Message for the last non-OK return on the calling thread ("" if none). */
 const char* fa_last_error(void);

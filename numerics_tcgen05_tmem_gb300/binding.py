@@ -23,9 +23,15 @@ FA_ERR_TIMEOUT = 4
 FA_ERR_DEVICE_BOUNDS = 5
 FA_WARN_NONFINITE = 6
 
+# which output a non-finite count belongs to (fa_device_report.nonfinite[i])
+FA_OUT_O, FA_OUT_LSE, FA_OUT_DQ, FA_OUT_DK, FA_OUT_DV = range(5)
+OUTPUT_NAMES = ("o", "lse", "dq", "dk", "dv")
+FA_DEVFLAG_TIMEOUT, FA_DEVFLAG_BOUNDS, FA_DEVFLAG_NONFINITE = 1, 2, 4
+
 # every symbol include/fa.h declares
 EXPORTS = ("fa_fwd", "fa_fwd_fp8", "fa_quantize_fp8", "fa_bwd", "fa_bwd_staged", "fa_bwd_noalloc",
-           "fa_bwd_workspace_size", "fa_device_status", "fa_last_error", "fa_version")
+           "fa_bwd_noalloc_status", "fa_bwd_workspace_size", "fa_device_status", "fa_device_report_read",
+           "fa_last_error", "fa_version")
 
 # size of the fixed device scratch behind fa_bwd_noalloc (FA_NOALLOC_SCRATCH_BYTES in fa.h)
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -43,6 +49,17 @@ class RowStats(ctypes.Structure):
     _fields_ = [("row_max_raw", ctypes.c_void_p), ("row_ties", ctypes.c_void_p),
                 ("row_branch", ctypes.c_void_p), ("row_ones", ctypes.c_void_p),
                 ("row_min_raw", ctypes.c_void_p)]
+
+
+class DeviceReport(ctypes.Structure):
+    """fa_device_report: flags, the first failed index check and non-finite counts per output."""
+    _fields_ = [("flags", ctypes.c_uint32), ("bounds_site", ctypes.c_uint32), ("bounds_value", ctypes.c_int64),
+                ("nonfinite", ctypes.c_uint64 * 5), ("reserved", ctypes.c_uint64)]
+
+    def as_dict(self):
+        return {"flags": int(self.flags), "bounds_site": int(self.bounds_site),
+                "bounds_value": int(self.bounds_value),
+                "nonfinite": {n: int(self.nonfinite[i]) for i, n in enumerate(OUTPUT_NAMES)}}
 
 
 _lib = None
@@ -73,6 +90,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.fa_bwd_noalloc.restype = ci
     L.fa_device_status.argtypes = [vp]
     L.fa_device_status.restype = ci
+    L.fa_device_report_read.argtypes = [vp, ctypes.POINTER(DeviceReport)]
+    L.fa_device_report_read.restype = ci
+    L.fa_bwd_noalloc_status.argtypes = [vp, ctypes.POINTER(DeviceReport)]
+    L.fa_bwd_noalloc_status.restype = ci
     L.fa_last_error.argtypes = []
     L.fa_last_error.restype = ctypes.c_char_p
     L.fa_version.argtypes = []
@@ -163,6 +184,20 @@ def fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, delta, causal: bool, scale: 
 
 def fa_device_status(stream=None) -> int:
     return load().fa_device_status(_stream(stream))
+
+
+def fa_device_report_read(stream=None):
+    """(status code, report dict) of the library's device status record; reading clears it."""
+    rep = DeviceReport()
+    rc = load().fa_device_report_read(_stream(stream), ctypes.byref(rep))
+    return rc, rep.as_dict()
+
+
+def fa_bwd_noalloc_status(stream=None):
+    """(status code, report dict) of fa_bwd_noalloc's own status record; reading clears it."""
+    rep = DeviceReport()
+    rc = load().fa_bwd_noalloc_status(_stream(stream), ctypes.byref(rep))
+    return rc, rep.as_dict()
 
 
 # ----------------------------------------------------------------- tensor-level helpers

@@ -5,7 +5,7 @@ the objects link into one shared library with the CUDA runtime linked
 statically, so loading the library needs no GPU and no libcuda (the driver's
 tensor-map encoder is looked up at run time).
 
-    python -m numerics_tcgen05_tmem_gb300.build [--testhooks]
+    python -m numerics_tcgen05_tmem_gb300.build [--testhooks | --debug-bounds]
 """
 from __future__ import annotations
 
@@ -24,6 +24,10 @@ LIB = os.path.join(HERE, "libfa.so")
 # after 100 ms.  Never loaded by the binding, the benchmark or the smoke check.
 LIB_TESTHOOKS = os.path.join(BUILD, "testhooks", "libfa_testhooks.so")
 TESTHOOKS_FLAGS = ["-DFA_TEST_HOOKS=1", "-DFA_WAIT_TIMEOUT_NS=100000000ull"]
+# Debug build: FA_DEBUG_BOUNDS checks the kernels' computed indices before each access and
+# records the first violation in the status record (it never traps).  Loaded only by its test.
+LIB_DEBUG_BOUNDS = os.path.join(BUILD, "debugbounds", "libfa_debugbounds.so")
+DEBUG_BOUNDS_FLAGS = ["-DFA_DEBUG_BOUNDS=1"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -49,12 +53,17 @@ def _needs_rebuild(extra_flags, lib=LIB, objdir=BUILD) -> bool:
     return any(os.path.getmtime(p) > t for p in deps if os.path.exists(p))
 
 
-def build(force: bool = False, verbose: bool = False, testhooks: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, testhooks: bool = False, debug_bounds: bool = False) -> str:
     extra = []
     lib, objdir = LIB, BUILD
+    if testhooks and debug_bounds:
+        raise ValueError("build one variant at a time")
     if testhooks:
         extra = extra + TESTHOOKS_FLAGS
         lib, objdir = LIB_TESTHOOKS, os.path.dirname(LIB_TESTHOOKS)
+    if debug_bounds:
+        extra = extra + DEBUG_BOUNDS_FLAGS
+        lib, objdir = LIB_DEBUG_BOUNDS, os.path.dirname(LIB_DEBUG_BOUNDS)
     if not force and not _needs_rebuild(extra, lib, objdir):
         return lib
     nvcc = nvcc_path()
@@ -76,7 +85,7 @@ def build(force: bool = False, verbose: bool = False, testhooks: bool = False) -
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = lib + ".tmp"
-    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
+    cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static", "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
@@ -90,9 +99,10 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--testhooks", action="store_true", help="build the failure-injection test library")
+    ap.add_argument("--debug-bounds", action="store_true", help="build the index-checking debug library")
     ap.add_argument("-v", "--verbose", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose, testhooks=a.testhooks))
+    print(build(force=a.force, verbose=a.verbose, testhooks=a.testhooks, debug_bounds=a.debug_bounds))
 
 
 if __name__ == "__main__":

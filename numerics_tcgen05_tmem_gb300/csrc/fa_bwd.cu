@@ -70,6 +70,7 @@ struct Cfg {
   static constexpr int kBarOff = kDeltaOff + kStages * kBlock * 4;
   static constexpr int kSmemBytes = kBarOff + 256;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 128, kTmemDK = 256, kTmemDV = 256 + D;
+  static_assert(kTmemDV + D <= 512 && kTmemDQ + D <= kTmemDK, "TMEM plan exceeds 512 columns");
   static constexpr uint32_t kIdescSq = idesc_bf16(128, kBlock, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescKV = idesc_bf16(128, D, false, true);        // dV (TMEM A), dK
   static constexpr uint32_t kIdescQ = idesc_bf16(128, D, true, true);          // dQ: A = dS (MN-major)
@@ -90,7 +91,7 @@ struct Params {
   float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  uint32_t* status;
+  DevStatus* status;
   int N;
   int BH;
   int N_pad;        // N rounded up to 128
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(256) fa_bwd_preprocess(const __nv_bfloat16* __
 // --------------------------------------------------------------------------- dQ convert
 __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict__ dq_acc,
                                                          __nv_bfloat16* __restrict__ dq, float scale,
-                                                         long long n8, uint32_t* status) {
+                                                         long long n8, DevStatus* status) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const bool in = i < n8;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
@@ -159,17 +160,15 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict
     a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
     b = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
   }
-  const float mx = fmaxf(fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))),
-                         fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-  report_nonfinite(!(mx < INFINITY) || (a.x != a.x) || (a.y != a.y) || (a.z != a.z) || (a.w != a.w) ||
-                       (b.x != b.x) || (b.y != b.y) || (b.z != b.z) || (b.w != b.w),
-                   status);
-  if (!in) return;
   uint4 out;
   out.x = pack_bf16x2(a.x * scale, a.y * scale);
   out.y = pack_bf16x2(a.z * scale, a.w * scale);
   out.z = pack_bf16x2(b.x * scale, b.y * scale);
   out.w = pack_bf16x2(b.z * scale, b.w * scale);
+  report_nonfinite(nonfinite_bf16x2(out.x) + nonfinite_bf16x2(out.y) + nonfinite_bf16x2(out.z) +
+                       nonfinite_bf16x2(out.w),
+                   status, kOutDq);
+  if (!in) return;
   reinterpret_cast<uint4*>(dq)[i] = out;
 }
 
@@ -184,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The swizzled operand layouts need a 1024-byte aligned base; there is no slack
   // for re-alignment at d = 128, so refuse to run rather than compute garbage.
   if (smem_u32(smem) & 1023u) {
-    if (threadIdx.x == 0) atomicOr(p.status, kDevBounds);
+    if (threadIdx.x == 0) report_bounds(p.status, kSiteSmemAlign, (long long)smem_u32(smem));
     return;
   }
   Bars& sh = *reinterpret_cast<Bars*>(smem + C::kBarOff);
@@ -214,6 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.mma_done, 1);
     mbar_init(&sh.never, 1);
     fence_barrier_init();
+    FA_BOUNDS_OK(C::kBarOff + sizeof(Bars) <= dynamic_smem_bytes(), p.status, kSiteBwdSmemSize,
+                 dynamic_smem_bytes());
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&sh.tmem_base, 512);
@@ -245,6 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (it / kStages) & 1;
         const int row0 = (i0 + it) * kBlock;
         if (!mbar_wait(&sh.q_empty[s], ph ^ 1, abort_flag, p.status)) break;
+        if (!FA_BOUNDS_OK(row0 < p.N_pad && (long long)stat_base + row0 + kBlock <= (long long)p.BH * p.N_pad,
+                          p.status, kSiteBwdQRow, row0))
+          break;
         // Q tile plus the tile's 128 padded lse*log2(e) and delta values (512 B each)
         mbar_arrive_expect_tx(&sh.q_full[s], C::kTileBytes + 2 * kBlock * 4);
         for (int c = 0; c < D / 64; ++c)
@@ -455,7 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           dsk[4 * gg + 2] = v4.z;
           dsk[4 * gg + 3] = v4.w;
           const uint32_t chunk = (uint32_t)(c0 / 8 + gg);
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ sw) << 4)) = v4;
+          if (FA_BOUNDS_OK(h * 16384 + r * 128 + (int)((chunk ^ sw) << 4) + 16 <= kBlock * kBlock * 2, p.status,
+                           kSiteBwdDsSmem, r))
+            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ sw) << 4)) = v4;
         }
         // packed columns [c0/2, c0/2 + 16) of this warpgroup's dP^T region: their dP^T values
         // (columns < c0 + 32) have already been read
@@ -476,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t = tmem + (h == 0 ? C::kTmemDK : C::kTmemDV) + lane_off;
       const float mul = h == 0 ? p.scale : 1.f;
       __nv_bfloat16* out = h == 0 ? p.dk : p.dv;
+      uint32_t bad = 0;  // NaN/Inf entries of this row, as stored
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t w[32];
@@ -484,20 +491,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence(w);
         uint4 pkd[4];
         uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
-        bool bad = false;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float g0 = __uint_as_float(w[2 * i]) * mul, g1 = __uint_as_float(w[2 * i + 1]) * mul;
-          bad |= !(fabsf(g0) < INFINITY) || !(fabsf(g1) < INFINITY);
           pw[i] = pack_bf16x2(g0, g1);
+          bad += nonfinite_bf16x2(pw[i]);
         }
-        report_nonfinite(bad && valid, p.status);
-        if (valid) {
+        if (valid && FA_BOUNDS_OK(orow + c0 + 32 <= (size_t)p.BH * p.N * D, p.status, kSiteBwdKVRow, key)) {
           uint4* dst = reinterpret_cast<uint4*>(out + orow + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
         }
       }
+      report_nonfinite(valid ? bad : 0u, p.status, h == 0 ? kOutDk : kOutDv);
     }
   } else {
     // ------------------------------------------------------------------ dQ warpgroup
@@ -534,13 +540,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) bulk_wait_read_but_one();
         named_barrier(1, kBlock);
         uint8_t* row = smem + C::kDQOff + (2 * pair + (r >> 6)) * C::kDQSlot + (r & 63) * 128;
+        if (FA_BOUNDS_OK((2 * pair + (r >> 6)) * C::kDQSlot + (r & 63) * 128 + 128 <= 4 * C::kDQSlot, p.status,
+                         kSiteBwdDqStage, r)) {
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(row + (((uint32_t)ch ^ sw) << 4)) =
-              make_uint4(w[g * 32 + ch * 4], w[g * 32 + ch * 4 + 1], w[g * 32 + ch * 4 + 2], w[g * 32 + ch * 4 + 3]);
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(row + (((uint32_t)ch ^ sw) << 4)) = make_uint4(
+                w[g * 32 + ch * 4], w[g * 32 + ch * 4 + 1], w[g * 32 + ch * 4 + 2], w[g * 32 + ch * 4 + 3]);
+        }
         fence_proxy_async_smem();
         named_barrier(1, kBlock);
-        if (leader) {
+        if (leader && FA_BOUNDS_OK(g * 32 + 32 <= D && q0 < p.N_pad && bh < p.BH, p.status, kSiteBwdDqCoord, q0)) {
           tma_reduce_add_3d(&tmDQ, smem + C::kDQOff + (2 * pair) * C::kDQSlot, g * 32, q0, bh);
           tma_reduce_add_3d(&tmDQ, smem + C::kDQOff + (2 * pair + 1) * C::kDQSlot, g * 32, q0 + 64, bh);
           bulk_commit_group();
@@ -595,7 +604,7 @@ Scratch carve_scratch(void* base, int B, int H, int N, int d) {
 template <int D>
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
                void* dk, void* dv, float* delta_out, int B, int H, int N, int causal, float scale,
-               const Scratch& sc, cudaStream_t stream, int stages, uint32_t* status_word = nullptr) {
+               const Scratch& sc, cudaStream_t stream, int stages, fa::DevStatus* status_word = nullptr) {
   using namespace fa;
   using C = bwd::Cfg<D>;
   const long long rows = (long long)B * H * N;
@@ -653,7 +662,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   }
   if (!(stages & FA_BWD_DQ_CONVERT)) return FA_OK;
   const long long n8 = rows * D / 8;
-  uint32_t* st_word = status_word ? status_word : device_status_word();
+  DevStatus* st_word = status_word ? status_word : device_status_word();
   if (!st_word) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
   bwd::fa_bwd_dq_convert<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(sc.dq_acc, static_cast<__nv_bfloat16*>(dq),
                                                                            scale, n8, st_word);
@@ -671,6 +680,7 @@ extern "C" int fa_bwd_staged(const void* q, const void* k, const void* v, const 
                              const void* dO, void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N,
                              int d, int causal, float scale, void* workspace, size_t workspace_bytes, void* stream,
                              int stages) {
+  fa::NvtxRange nvtx_range("fa_bwd_staged");
   using namespace fa;
   clear_error();
   int rc;
@@ -700,6 +710,7 @@ extern "C" int fa_bwd_staged(const void* q, const void* k, const void* v, const 
 extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                       void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N, int d, int causal,
                       float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  fa::NvtxRange nvtx_range("fa_bwd");
   return fa_bwd_staged(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, d, causal, scale, workspace,
                        workspace_bytes, stream, FA_BWD_ALL);
 }
@@ -719,18 +730,19 @@ constexpr size_t kNoAllocScratchBytes = FA_NOALLOC_SCRATCH_BYTES;
 constexpr int kNoAllocMaxDevices = 64;
 
 // Scratch shared by every fa_bwd_noalloc call on a device, plus that entry point's own
-// device status word (the library's allocated status word is not used here).
+// device status record (the library's allocated record is not used here; it is read with
+// fa_bwd_noalloc_status).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-static __device__ __align__(256) uint32_t g_noalloc_status;
+static __device__ __align__(256) fa::DevStatus g_noalloc_status;
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-uint32_t* g_noalloc_status_ptr[kNoAllocMaxDevices] = {};
+fa::DevStatus* g_noalloc_status_ptr[kNoAllocMaxDevices] = {};
 
 // Device address of the static scratch for the current device.  In host code the array's
 // name is only a host-side stand-in, so the address must come from cudaGetSymbolAddress,
 // once per device, with that device current.
-int noalloc_scratch(void** scratch, uint32_t** status) {
+int noalloc_scratch(void** scratch, fa::DevStatus** status) {
   int dev = 0;
   int rc = fa::check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
   if (rc) return rc;
@@ -743,7 +755,7 @@ int noalloc_scratch(void** scratch, uint32_t** status) {
     if ((rc = fa::check_cuda(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)"))) return rc;
     if ((rc = fa::check_cuda(cudaGetSymbolAddress(&s, g_noalloc_status), "cudaGetSymbolAddress(status)"))) return rc;
     g_noalloc_ptr[dev] = p;
-    g_noalloc_status_ptr[dev] = static_cast<uint32_t*>(s);
+    g_noalloc_status_ptr[dev] = static_cast<fa::DevStatus*>(s);
   }
   *scratch = g_noalloc_ptr[dev];
   *status = g_noalloc_status_ptr[dev];
@@ -755,6 +767,7 @@ int noalloc_scratch(void** scratch, uint32_t** status) {
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                               const void* dO, void* dq, void* dk, void* dv, float* delta_out, int B, int H, int N,
                               int d, int causal, float scale, void* stream) {
+  fa::NvtxRange nvtx_range("fa_bwd_noalloc");
   using namespace fa;
   clear_error();
   int rc;
@@ -773,7 +786,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                      "(use fa_bwd with a caller-allocated workspace)",
                      need, kNoAllocScratchBytes);
   void* scratch = nullptr;
-  uint32_t* status = nullptr;
+  DevStatus* status = nullptr;
   if ((rc = noalloc_scratch(&scratch, &status))) return rc;
   const Scratch sc = carve_scratch(scratch, B, H, N, d);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -781,4 +794,14 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
                                   FA_BWD_ALL, status)
                  : launch_bwd<128>(q, k, v, o, lse, dO, dq, dk, dv, delta_out, B, H, N, causal ? 1 : 0, scale, sc, s,
                                    FA_BWD_ALL, status);
+}
+
+extern "C" int fa_bwd_noalloc_status(void* stream, fa_device_report* out) {
+  fa::NvtxRange nvtx_range("fa_bwd_noalloc_status");
+  fa::clear_error();
+  void* scratch = nullptr;
+  fa::DevStatus* status = nullptr;
+  int rc = noalloc_scratch(&scratch, &status);
+  if (rc) return rc;
+  return fa::read_and_clear_status(status, stream, out);
 }

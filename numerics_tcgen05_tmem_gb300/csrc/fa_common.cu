@@ -1,5 +1,5 @@
 // Host-side common code: thread-local error messages, the per-device status
-// word, tensor-map encoding through the driver entry point, fa_device_status.
+// record, tensor-map encoding through the driver entry point, fa_device_status.
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -31,7 +31,7 @@ int check_cuda(cudaError_t e, const char* what) {
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-uint32_t* g_status[kMaxDevices] = {};
+DevStatus* g_status[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -40,17 +40,43 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 EncodeTiledFn g_encode = nullptr;
 }  // namespace
 
-uint32_t* device_status_word() {
+DevStatus* device_status_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_status[dev]) {
-    uint32_t* p = nullptr;
-    if (cudaMalloc(&p, sizeof(uint32_t)) != cudaSuccess) return nullptr;
-    if (cudaMemset(p, 0, sizeof(uint32_t)) != cudaSuccess) return nullptr;
+    DevStatus* p = nullptr;
+    if (cudaMalloc(&p, sizeof(DevStatus)) != cudaSuccess) return nullptr;
+    if (cudaMemset(p, 0, sizeof(DevStatus)) != cudaSuccess) return nullptr;
     g_status[dev] = p;
   }
   return g_status[dev];
+}
+
+static_assert(sizeof(DevStatus) == sizeof(fa_device_report), "device record and public report differ");
+
+int read_and_clear_status(void* dev_rec, void* stream, fa_device_report* out) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc = check_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  if (rc) return rc;
+  DevStatus v;
+  rc = check_cuda(cudaMemcpy(&v, dev_rec, sizeof(v), cudaMemcpyDeviceToHost), "read status record");
+  if (rc) return rc;
+  if (out) memcpy(out, &v, sizeof(v));
+  if (v.flags) {
+    rc = check_cuda(cudaMemset(dev_rec, 0, sizeof(DevStatus)), "clear status record");
+    if (rc) return rc;
+  }
+  if (v.flags & kDevTimeout) return set_error(FA_ERR_TIMEOUT, "a kernel's bounded wait timed out");
+  if (v.flags & kDevBounds)
+    return set_error(FA_ERR_DEVICE_BOUNDS, "a device-side index check failed (site %u, index %lld)", v.bounds_site,
+                     v.bounds_value);
+  if (v.flags & kDevNonFinite)
+    return set_error(FA_WARN_NONFINITE,
+                     "outputs held NaN or Inf (entries: O %llu, LSE %llu, dQ %llu, dK %llu, dV %llu)",
+                     v.nonfinite[kOutO], v.nonfinite[kOutLse], v.nonfinite[kOutDq], v.nonfinite[kOutDk],
+                     v.nonfinite[kOutDv]);
+  return FA_OK;
 }
 
 int sm_count() {
@@ -118,23 +144,21 @@ int check_ptr(const void* p, const char* name) {
 
 }  // namespace fa
 
+extern "C" int fa_device_report_read(void* stream, fa_device_report* out) {
+  fa::NvtxRange nvtx_range("fa_device_report_read");
+  fa::clear_error();
+  if (!out) return fa::set_error(FA_ERR_INVALID_ARG, "out is NULL");
+  fa::DevStatus* w = fa::device_status_word();
+  if (!w) return fa::set_error(FA_ERR_CUDA, "status record unavailable");
+  return fa::read_and_clear_status(w, stream, out);
+}
+
 extern "C" int fa_device_status(void* stream) {
-  uint32_t* w = fa::device_status_word();
-  if (!w) return fa::set_error(FA_ERR_CUDA, "status word unavailable");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int rc = fa::check_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize");
-  if (rc) return rc;
-  uint32_t v = 0;
-  rc = fa::check_cuda(cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost), "read status word");
-  if (rc) return rc;
-  if (v) {
-    rc = fa::check_cuda(cudaMemset(w, 0, sizeof(uint32_t)), "clear status word");
-    if (rc) return rc;
-  }
-  if (v & fa::kDevTimeout) return fa::set_error(FA_ERR_TIMEOUT, "a kernel's bounded wait timed out");
-  if (v & fa::kDevBounds) return fa::set_error(FA_ERR_DEVICE_BOUNDS, "a device-side layout check failed");
-  if (v & fa::kDevNonFinite) return fa::set_error(FA_WARN_NONFINITE, "an output held NaN or Inf");
-  return FA_OK;
+  fa::NvtxRange nvtx_range("fa_device_status");
+  fa::clear_error();
+  fa::DevStatus* w = fa::device_status_word();
+  if (!w) return fa::set_error(FA_ERR_CUDA, "status record unavailable");
+  return fa::read_and_clear_status(w, stream, nullptr);
 }
 
 extern "C" const char* fa_last_error(void) { return fa::g_last_error; }

@@ -90,6 +90,7 @@ struct Cfg {
   static constexpr uint32_t kIdescS = kFp8 ? idesc_e4m3(128, kBlockN, false, false) : idesc_bf16(128, kBlockN, false, false);
   static constexpr uint32_t kIdescO = kFp8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
   static_assert(kAtoms >= 1 && kAtoms * kAtomBytes == D * kElem, "tile rows must be whole swizzle atoms");
+  static_assert((kRing ? 3 : 2) * 128 <= kTmemO0 && kTmemO1 + D <= 512, "TMEM plan exceeds 512 columns");
   // shared-memory descriptor of an operand in this tile layout (8-row groups kAtomBytes * 8 apart)
   __device__ static uint64_t sdesc(uint32_t saddr, uint32_t lbo) {
     return kAtomBytes == 128 ? sdesc_sw128(saddr, lbo, 8 * kAtomBytes) : sdesc_sw64(saddr, lbo, 8 * kAtomBytes);
@@ -111,7 +112,7 @@ struct Params {
   int8_t* stat_branch;
   int32_t* stat_ones;
   float* stat_min;
-  uint32_t* status;
+  DevStatus* status;
   int N;
   int BH;
   int n_qblocks;   // ceil(N / 256)
@@ -206,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.mma_done, 1);
     mbar_init(&sh.never, 1);
     fence_barrier_init();
+    FA_BOUNDS_OK((uint32_t)(smem - smem_raw) + C::kVOff + C::kStages * C::kTileBytes <= dynamic_smem_bytes(),
+                 p.status, kSiteFwdSmemSize, dynamic_smem_bytes());
   }
   if (warp == kMmaWarp) {
     tmem_alloc(&sh.tmem_base, 512);
@@ -228,14 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ntiles = (nb1 > 0) ? 2 : 1;
       mbar_arrive_expect_tx(&sh.q_full, ntiles * C::kTileBytes);
       for (int t = 0; t < ntiles; ++t)
-        for (int c = 0; c < C::kAtoms; ++c)
-          tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * C::kAtomBlock, &tmQ, &sh.q_full, c * C::kAtomElems,
-                      qb * (kTiles * kBlockM) + t * kBlockM, bh);
+        if (FA_BOUNDS_OK(qb * (kTiles * kBlockM) + t * kBlockM < p.N, p.status, kSiteFwdQRow,
+                         qb * (kTiles * kBlockM) + t * kBlockM))
+          for (int c = 0; c < C::kAtoms; ++c)
+            tma_load_3d(smem + C::kQOff + t * C::kTileBytes + c * C::kAtomBlock, &tmQ, &sh.q_full,
+                        c * C::kAtomElems, qb * (kTiles * kBlockM) + t * kBlockM, bh);
       int nk_issued = 0, nv_issued = 0;
       for (int j = 0; j < nbmax; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
         if (!mbar_wait(&sh.k_empty[s], ph ^ 1, abort_flag, p.status)) break;
+        if (!FA_BOUNDS_OK(j * kBlockN < p.N, p.status, kSiteFwdKVRow, j * kBlockN)) break;
         mbar_arrive_expect_tx(&sh.k_full[s], C::kTileBytes);
         for (int c = 0; c < C::kAtoms; ++c)
           tma_load_3d(smem + C::kKOff + s * C::kTileBytes + c * C::kAtomBlock, &tmK, &sh.k_full[s], c * C::kAtomElems,
@@ -297,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = k_lo; kk < k_hi; ++kk) {
           // a k-step covers 32 / kElem keys, one atom row (kAtomBytes) each; LBO = the next
           // atom column block along d (only with two or more)
+          FA_BOUNDS_OK((kk + 1) * (32 / C::kElem) * C::kAtomBytes <= C::kAtomBlock && s < C::kStages, p.status,
+                       kSiteFwdVDesc, kk);
           const uint64_t bd = C::sdesc(b0 + kk * (32 / C::kElem) * C::kAtomBytes, C::kAtomBlock);
           if constexpr (kFp8)
             mma_ts_f8(d, a + kk * 8, bd, C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
@@ -429,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(&sh.s_full[t][ev_slot<C::kRing>(j)], ev_parity<C::kRing>(j), abort_flag, p.status))) break;
       tc_fence_after();
       const uint32_t tS = C::kRing ? tmem + C::s_col(t, j) + lane_off : tS_fixed;  // this block's S, then P~
+      FA_BOUNDS_OK(C::s_col(t, j) + kBlockN <= C::kTmemO0, p.status, kSiteFwdTmemS, C::s_col(t, j));
       // the whole 128-column row in one round trip: four loads, one wait; each load also
       // returns the largest of its 32 raw scores
       uint32_t raw[kBlockN];
@@ -636,8 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // FP8: l sums P~ * 2^8
       const float lse_row = kFp8 ? m * (p.scale * dqk) + (logf(l) - (float)kPScaleLog2 * 0.6931471805599453f)
                                  : m * p.scale + logf(l);
-      report_nonfinite(row < p.N && !(fabsf(lse_row) < INFINITY), p.status);
-      if (row < p.N) {
+      report_nonfinite((row < p.N && !(fabsf(lse_row) < INFINITY)) ? 1u : 0u, p.status, kOutLse);
+      if (row < p.N &&
+          FA_BOUNDS_OK((long long)bh * p.N + row < (long long)p.BH * p.N, p.status, kSiteFwdLseRow, row)) {
         const size_t srow = (size_t)bh * p.N + row;
         p.lse[srow] = lse_row;
         if constexpr (kStats) {
@@ -703,6 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < p.N;
       const size_t orow = ((size_t)bh * p.N + (valid ? row : 0)) * D;
       const uint32_t tO = tmem + (t == 0 ? C::kTmemO0 : C::kTmemO1) + ((uint32_t)lane_base << 16);
+      uint32_t bad = 0;  // NaN/Inf entries of this row of O, as stored
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t w[32];
@@ -711,20 +722,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence(w);
         uint4 pkd[4];
         uint32_t* pw = reinterpret_cast<uint32_t*>(pkd);
-        bool bad = false;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float o0 = __uint_as_float(w[2 * i]) * inv_l, o1 = __uint_as_float(w[2 * i + 1]) * inv_l;
-          bad |= !(fabsf(o0) < INFINITY) || !(fabsf(o1) < INFINITY);
           pw[i] = pack_bf16x2(o0, o1);
+          bad += nonfinite_bf16x2(pw[i]);
         }
-        report_nonfinite(bad && valid, p.status);
-        if (valid) {
+        if (valid && FA_BOUNDS_OK(orow + c0 + 32 <= (size_t)p.BH * p.N * D, p.status, kSiteFwdORow, row)) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + orow + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
         }
       }
+      report_nonfinite(valid ? bad : 0u, p.status, kOutO);
     }
   }
 
@@ -818,6 +828,7 @@ int prepare_fwd(fa::fwd::Params& p, bool& want_stats, const void* q, const void*
 
 extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
                       int causal, float scale, int stable, float beta, const fa_row_stats* stats, void* stream) {
+  fa::NvtxRange nvtx_range("fa_fwd");
   using namespace fa;
   clear_error();
   fwd::Params p;
@@ -836,6 +847,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
 extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* descale, void* o, float* lse,
                           int B, int H, int N, int d, int causal, float scale, int stable, float beta,
                           const fa_row_stats* stats, void* stream) {
+  fa::NvtxRange nvtx_range("fa_fwd_fp8");
   using namespace fa;
   clear_error();
   if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);

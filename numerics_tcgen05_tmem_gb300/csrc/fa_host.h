@@ -1,5 +1,5 @@
 // Host-side helpers shared by the entry points: error reporting, the per-device
-// status word, tensor-map encoding and argument checks.
+// status record, tensor-map encoding and argument checks.
 #pragma once
 
 #include <cuda.h>
@@ -7,9 +7,21 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/fa.h"
 
 namespace fa {
+
+// An NVTX range around one entry point's host work (argument checks, tensor maps, launches),
+// so a profiler's timeline shows each ABI call; without a profiler attached it costs a call
+// into a no-op stub.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Record `msg` as this thread's last error and return `code`.
 int set_error(int code, const char* fmt, ...);
@@ -18,8 +30,16 @@ void clear_error();
 // Returns FA_ERR_CUDA (with the CUDA message recorded) if e != cudaSuccess.
 int check_cuda(cudaError_t e, const char* what);
 
-// The current device's status word (allocated on first use); nullptr on failure.
-uint32_t* device_status_word();
+struct DevStatus;
+
+// The current device's status record (allocated and zeroed on first use); nullptr on failure.
+DevStatus* device_status_word();
+
+// Synchronise `stream`, copy the status record at `dev_rec` (a device address) into `out`,
+// clear it on the device when anything was set, and map its flags to an fa_status code
+// (FA_ERR_TIMEOUT, FA_ERR_DEVICE_BOUNDS, FA_WARN_NONFINITE in that order of precedence).
+// Allocates nothing.
+int read_and_clear_status(void* dev_rec, void* stream, fa_device_report* out);
 
 // Encode a 3-D BF16 tensor map over a contiguous [BH, N, d] tensor with a
 // 128-byte swizzle and a (64 x box_rows x 1) box; out-of-range rows read as zero.

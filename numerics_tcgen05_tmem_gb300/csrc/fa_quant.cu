@@ -89,6 +89,7 @@ __global__ void finalize_kernel(float* descale) {
 }  // namespace fa
 
 extern "C" int fa_quantize_fp8(const void* x, size_t n, void* x8, float* descale, void* stream) {
+  fa::NvtxRange nvtx_range("fa_quantize_fp8");
   using namespace fa;
   clear_error();
   int rc;

@@ -11,19 +11,86 @@
 
 namespace fa {
 
-// ----------------------------------------------------------------- status word
-// Device-side errors are OR-ed into a status word that the host reads back.
+// ----------------------------------------------------------------- status record
+// Device-side errors are OR-ed into the flags of a status record that the host reads back
+// (its layout is fa_device_report of the public header).
 enum : uint32_t {
   kDevOk = 0,
   kDevTimeout = 1u << 0,   // a bounded wait on an mbarrier ran out
-  kDevBounds = 1u << 1,    // a device-side layout check failed
+  kDevBounds = 1u << 1,    // a device-side index or layout check failed
   kDevNonFinite = 1u << 2, // an output value was NaN or Inf
 };
 
-// Record kDevNonFinite once per warp if any lane saw a non-finite output value.  All 32
-// lanes of the warp must call it (it votes across the warp).
-__device__ __forceinline__ void report_nonfinite(bool bad, uint32_t* status) {
-  if (__any_sync(0xffffffffu, bad) && (threadIdx.x % 32) == 0) atomicOr(status, kDevNonFinite);
+// Which output a non-finite count belongs to (index into DevStatus::nonfinite).
+enum : int { kOutO = 0, kOutLse = 1, kOutDq = 2, kOutDk = 3, kOutDv = 4, kNumOuts = 5 };
+
+struct DevStatus {
+  uint32_t flags;                          // kDev* bits
+  uint32_t bounds_site;                    // first failed index check: its site id (0 = none)
+  long long bounds_value;                  // ... and the index it saw
+  unsigned long long nonfinite[kNumOuts];  // entries of each output that held NaN or Inf
+  unsigned long long reserved;
+};
+static_assert(sizeof(DevStatus) == 64, "status record layout");
+
+// Count `bad` non-finite entries of output `which`: the warp sums its lanes' counts and one
+// lane adds them to the record.  All 32 lanes of the warp must call it.
+__device__ __forceinline__ void report_nonfinite(uint32_t bad, DevStatus* status, int which) {
+  const uint32_t total = __reduce_add_sync(0xffffffffu, bad);
+  if (total != 0 && (threadIdx.x % 32) == 0) {
+    atomicAdd(&status->nonfinite[which], (unsigned long long)total);
+    atomicOr(&status->flags, kDevNonFinite);
+  }
+}
+
+// Number of NaN/Inf halves of a packed BF16 pair (exponent field all ones).
+__device__ __forceinline__ uint32_t nonfinite_bf16x2(uint32_t w) {
+  const uint32_t e = w & 0x7F807F80u;
+  return ((e & 0xFFFFu) == 0x7F80u ? 1u : 0u) + ((e >> 16) == 0x7F80u ? 1u : 0u);
+}
+
+// Site ids of the device-side index checks (fa_device_report.bounds_site).  The alignment
+// check is always compiled; the others only in builds with FA_DEBUG_BOUNDS, where the
+// computed global, shared-memory, tensor-memory and TMA indices are checked before use (the
+// fixed tensor-memory plans are checked at compile time).
+enum : uint32_t {
+  kSiteSmemAlign = 1,      // backward: dynamic shared memory not 1024-byte aligned
+  kSiteFwdSmemSize = 10,   // forward: the tile layout does not fit the dynamic shared memory
+  kSiteFwdQRow = 11,       // forward: a Q tile's first row is not below N
+  kSiteFwdKVRow = 12,      // forward: a K/V block's first row is not below N
+  kSiteFwdTmemS = 13,      // forward: an S / P~ buffer runs past the 512 TMEM columns
+  kSiteFwdORow = 14,       // forward: an O row write runs past the output
+  kSiteFwdLseRow = 15,     // forward: an LSE / statistics index runs past [B*H*N]
+  kSiteFwdVDesc = 16,      // forward: a V operand address leaves its ring stage
+  kSiteBwdSmemSize = 20,   // backward: the layout does not fit the dynamic shared memory
+  kSiteBwdQRow = 21,       // backward: a Q / dO tile row or its lse/delta slice is out of range
+  kSiteBwdDsSmem = 22,     // backward: a dS^T row store leaves the dS^T tile
+  kSiteBwdDqStage = 23,    // backward: a dQ staging row leaves the staging ring
+  kSiteBwdDqCoord = 24,    // backward: a dQ reduce-add box starts outside the accumulator
+  kSiteBwdKVRow = 25,      // backward: a dK / dV row write runs past the output
+};
+
+// Record a failed index check: the flag, and the site and index of the first one seen.
+__device__ __forceinline__ void report_bounds(DevStatus* status, uint32_t site, long long value) {
+  if (atomicCAS(&status->bounds_site, 0u, site) == 0u) status->bounds_value = value;
+  atomicOr(&status->flags, kDevBounds);
+}
+
+// FA_BOUNDS_OK(cond, status, site, value): in FA_DEBUG_BOUNDS builds, true when cond holds;
+// otherwise it records the violation (never traps) and is false, so the caller skips the
+// access.  In other builds it is the constant true and the check compiles away.
+#ifdef FA_DEBUG_BOUNDS
+#define FA_BOUNDS_OK(cond, status, site, value) \
+  ((cond) ? true : (::fa::report_bounds((status), (site), (long long)(value)), false))
+#else
+#define FA_BOUNDS_OK(cond, status, site, value) true
+#endif
+
+// Bytes of dynamic shared memory this CTA was launched with.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+  return n;
 }
 
 // Three-input minimum (sm_100+).
@@ -91,9 +158,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity to complete.  Returns false
 // when the CTA-wide abort flag is raised (by this or another warp) or when the
 // wait exceeds FA_WAIT_TIMEOUT_NS; in the latter case it raises the abort flag
-// and records kDevTimeout in the global status word.  Never spins forever.
+// and records kDevTimeout in the global status record.  Never spins forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                          uint32_t* status) {
+                                          DevStatus* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
@@ -103,7 +170,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > FA_WAIT_TIMEOUT_NS) {
       *abort_flag = 1u;
-      atomicOr(status, kDevTimeout);
+      atomicOr(&status->flags, kDevTimeout);
       return false;
     }
   }

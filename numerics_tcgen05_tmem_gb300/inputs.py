@@ -223,6 +223,27 @@ def random_case(B: int, H: int, N: int, d: int, causal: bool, seed: int, std: fl
                     _bf16(do), causal, s, stable, beta, {"B": B, "H": H, "N": N, "d": d})
 
 
+def tiny_tail_rows(N: int = 32768, d: int = 64, H: int = 1, tail_score: float = -178.0) -> Workload:
+    """Rows whose softmax denominator is one exact 1.0 plus N - 1 tiny terms.
+
+    Every query row is e_0 (1 in channel 0); key 0 is the zero vector (raw score 0, the
+    row's unique maximum) and every other key is tail_score * e_0, so each row sees one
+    score 0 and N - 1 scores tail_score.  At d = 64 (scale 1/8) the tiny terms are
+    exp(-22.25) ~ 2^-32: a 128-key block of them sums to less than half an FP32 ulp of 1,
+    the case that separates a compensated cross-block row sum from a plain one.
+    Non-causal; V and dO are N(0, 1), seeded.
+    """
+    rng = np.random.default_rng(BASE_SEED + 5)
+    q = np.zeros((1, H, N, d), dtype=np.float32)
+    q[..., 0] = 1.0
+    k = np.zeros((1, H, N, d), dtype=np.float32)
+    k[:, :, 1:, 0] = tail_score
+    v = _normal(rng, (1, H, N, d))
+    do = _normal(rng, (1, H, N, d))
+    return Workload(f"tiny_tail_N{N}d{d}", _bf16(q), _bf16(k), _bf16(v), _bf16(do), False, 1.0 / math.sqrt(d), 1,
+                    1.25, {"B": 1, "H": H, "N": N, "d": d})
+
+
 WORKLOADS = {
     "tiny_ties": tiny_ties,
     "gpt2_small": gpt2_small,

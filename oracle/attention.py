@@ -205,7 +205,7 @@ def _fp32_exact(q_row: np.ndarray, k_row: np.ndarray) -> bool:
     return float(np.abs(nz).sum()) < g * 2.0 ** 24
 
 
-def decidable_rows(q, k, causal: bool, b: int = 0, h: int = 0, safety: float = 2.0):
+def decidable_rows(q, k, causal: bool, b: int = 0, h: int = 0, safety: float = 2.0, row_block: int = 256):
     """Which rows' (rm, rs, branch) an FP32 computation must reproduce exactly.
 
     A row is decidable when (a) the gap between its maximum and the next
@@ -213,31 +213,37 @@ def decidable_rows(q, k, causal: bool, b: int = 0, h: int = 0, safety: float = 2
     FP32 error bounds, and (b) every tied maximum comes from a bit-identical
     key row or is exact in FP32 whatever the summation order.  Returns
     (decidable [N] bool, bound [N] error bound of the maximum entry).
+    Rows are taken ``row_block`` at a time only to bound memory and time; each
+    row's decision uses that row alone.
     """
     q, k = _f64(q), _f64(k)
-    N = q.shape[2]
+    N, d = q.shape[2], q.shape[3]
     qb, kb = q[b, h], k[b, h]
+    u = 2.0 ** -24
+    gamma = d * u / (1.0 - d * u)
     dec = np.zeros(N, dtype=bool)
     bound = np.zeros(N)
-    for i in range(N):
-        js = np.arange(N) if not causal else np.arange(i + 1)
-        s = kb[js] @ qb[i]
-        err = fp32_dot_error_bound(qb[i], kb[js])
-        rm = s.max()
-        at_max = js[s == rm]
-        bound[i] = err[s == rm].max()
-        below = s < rm
-        ok = True
-        if below.any():
-            nxt = s[below].max()
-            e_next = err[below][s[below] == nxt].max()
-            ok = (rm - nxt) > safety * (bound[i] + e_next)
-        if ok and len(at_max) > 1:
-            ref = kb[at_max[0]]
-            for j in at_max[1:]:
+    abs_k = np.abs(kb)
+    for r0 in range(0, N, row_block):
+        rows = np.arange(r0, min(N, r0 + row_block))
+        vis = visible(rows, N, causal)
+        s = np.where(vis, qb[rows] @ kb.T, -np.inf)
+        err = gamma * (np.abs(qb[rows]) @ abs_k.T)           # fp32_dot_error_bound per entry
+        rm = s.max(axis=1)
+        at_max = vis & (s == rm[:, None])
+        bound[rows] = np.where(at_max, err, -np.inf).max(axis=1)
+        below = vis & (s < rm[:, None])
+        nxt = np.where(below, s, -np.inf).max(axis=1)
+        has_below = below.any(axis=1)
+        e_next = np.where(below & (s == nxt[:, None]), err, -np.inf).max(axis=1)
+        ok = ~has_below | ((rm - nxt) > safety * (bound[rows] + e_next))
+        for t in np.nonzero(ok & (at_max.sum(axis=1) > 1))[0]:
+            i = rows[t]
+            js = np.nonzero(at_max[t])[0]
+            ref = kb[js[0]]
+            for j in js[1:]:
                 if not np.array_equal(kb[j], ref) and not (_fp32_exact(qb[i], kb[j]) and _fp32_exact(qb[i], ref)):
-                    ok = False
+                    ok[t] = False
                     break
-        dec[i] = ok
+        dec[rows] = ok
     return dec, bound
-

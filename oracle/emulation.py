@@ -33,7 +33,9 @@ Readings where the pages are silent:
     m_j = max(m_{j-1}, rule(rowmax S_j, count in S_j)); it depends on the
     block width.
   * l accumulates the FP32 P~ (before the BF16 cast): the softmax stays in
-    FP32 and only the product with V is cast.
+    FP32 and only the product with V is cast.  Across blocks it is a Kahan
+    (compensated) sum by default, the summation the same page (§7.2) recommends
+    for the softmax denominator of large models.
   * FP8 forward (same page, §6.1: the shift carries over to FP8 with dynamic
     scaling): P~ is multiplied by 2^8 and rounded to E4M3 (nearest, ties to
     even) for the P~V product; l still sums the FP32 P~.
@@ -45,7 +47,9 @@ Readings where the pages are silent:
 Parity status: pinned in ``tests/test_emulation_pins.py`` -- in FP64 mode the
 blocked recurrence equals the one-shot oracle for every block width; the
 running tie state equals the whole-row state; plain mode produces exact-1.0
-entries at repeated maxima and stable mode removes them.
+entries at repeated maxima and stable mode removes them; on rows whose block
+sums fall below half an ulp of l, the uncompensated FP32 row sum drifts by the
+lost sums while the compensated one stays at the FP64 closed form.
 """
 from __future__ import annotations
 
@@ -82,7 +86,7 @@ def _rule32(rm, rs, beta32, stable):
 
 
 def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: float = 1.25,
-                    block_n: int = 128, precision: str = "bf16"):
+                    block_n: int = 128, precision: str = "bf16", compensated: bool = True):
     """Blocked online-softmax forward over key blocks of width ``block_n``.
 
     precision="bf16": FP32 state, P~ rounded to BF16 for P~V, O rounded to BF16.
@@ -90,6 +94,11 @@ def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: 
     forward; pass the dequantised Q, K, V).
     precision="fp64": the same recurrence with every value in FP64 and no
     rounding (used to pin the recurrence against the one-shot definition).
+    compensated: in FP32, the row sum l = alpha l + rowsum(P~) is accumulated across
+    blocks with Kahan's compensated summation (ijyty.com §7.2 recommends it for the
+    softmax denominator of large models): a compensation c carries the low-order part
+    each update loses, scaled by alpha with the sum, and the final row sum is l - c.
+    With compensated=False the update is the plain FP32 recurrence.
 
     Returns dict(o, lse, rm, rs, branch, m, ones) per [B, H, N]; ``ones`` is
     the number of visible P~ entries of a row whose rounded value (BF16, or
@@ -116,6 +125,7 @@ def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: 
             rs = np.zeros(N, dtype=np.int64)
             m = np.full(N, -np.inf, dtype=ft)
             l = np.zeros(N, dtype=ft)
+            lc = np.zeros(N, dtype=ft)          # Kahan compensation of l (FP32 paths)
             acc = np.zeros((N, dv), dtype=ft)
             ones = np.zeros(N, dtype=np.int64)
             br = np.zeros(N, dtype=np.int8)
@@ -155,7 +165,14 @@ def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: 
                         pb = (decode_e4m3(encode_e4m3((p * ps).astype(np.float32))) / float(ps)).astype(np.float32)
                     ones += ((pb == np.float32(1.0)) & vis).sum(axis=1)
                     rowsum = p.sum(axis=1, dtype=np.float32)
-                    l = (alpha * l).astype(ft) + rowsum
+                    ls = (alpha * l).astype(ft)
+                    if compensated:
+                        y = (rowsum - (alpha * lc).astype(ft)).astype(ft)
+                        t = (ls + y).astype(ft)
+                        lc = ((t - ls).astype(ft) - y).astype(ft)
+                        l = t
+                    else:
+                        l = (ls + rowsum).astype(ft)
                     pv = (pb.astype(np.float64) @ v[b, h, cols]).astype(ft)
                     acc = (alpha[:, None] * acc).astype(ft) + pv
                 else:
@@ -163,6 +180,8 @@ def blocked_forward(q, k, v, scale: float, causal: bool, stable: int = 0, beta: 
                     l = alpha * l + p.sum(axis=1)
                     acc = alpha[:, None] * acc + p @ v[b, h, cols]
                 m = m_new
+            if low:
+                l = (l - lc).astype(ft)
             o = acc / l[:, None]
             if low:
                 o = round_bf16(o.astype(np.float32))

@@ -102,3 +102,18 @@ def test_fp8_invalid_arguments(lib):
     assert lib.fa_quantize_fp8(good, 16, ctypes.c_void_p((1 << 20) + 4), ds, None) == binding.FA_ERR_INVALID_ARG
     assert lib.fa_quantize_fp8(good, 16, good, None, None) == binding.FA_ERR_INVALID_ARG
     assert b"descale" in lib.fa_last_error()
+
+
+def test_device_report_layout_matches_header():
+    # fa_device_report: flags, bounds_site, bounds_value, nonfinite[5], reserved -> 64 bytes
+    assert ctypes.sizeof(binding.DeviceReport) == 64
+    assert binding.DeviceReport.nonfinite.offset == 16
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    for name, val in (("FA_OUT_O", 0), ("FA_OUT_LSE", 1), ("FA_OUT_DQ", 2), ("FA_OUT_DK", 3), ("FA_OUT_DV", 4)):
+        assert re.search(rf"\b{name} = {val}\b", src), name
+        assert getattr(binding, name) == val
+
+
+def test_report_reader_rejects_null_output(lib):
+    assert lib.fa_device_report_read(None, None) == binding.FA_ERR_INVALID_ARG
+    assert b"out is NULL" in lib.fa_last_error()

@@ -76,18 +76,21 @@ def test_ragged_shapes(N, d, causal):
     check(w, run_fwd_bwd(w), oracle_grads(w))
 
 
-def test_llama7b_full_size_sampled_heads():
+@pytest.mark.parametrize("stable", [0, 1])
+def test_llama7b_full_size_sampled_heads(stable):
+    # the backward after a plain or a stabilised forward (it reads only O and LSE)
     w = inputs.llama7b_long()
-    res = run_fwd_bwd(w)
+    res = run_fwd_bwd(w, stable)
     heads = [0, 31]
     ws = inputs.llama7b_long(heads=heads)
     check(ws, res, oracle_grads(ws), sel=lambda t: t[:, heads])
 
 
+@pytest.mark.parametrize("stable", [0, 1])
 @pytest.mark.parametrize("causal", [True, False])
-def test_extreme_16k_sampled_head(causal):
+def test_extreme_16k_sampled_head(causal, stable):
     w = inputs.extreme_16k(causal=causal)
-    res = run_fwd_bwd(w)
+    res = run_fwd_bwd(w, stable)
     ws = inputs.extreme_16k(causal=causal, heads=[9])
     check(ws, res, oracle_grads(ws), sel=lambda t: t[:, [9]])
 

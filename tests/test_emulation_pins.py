@@ -132,3 +132,35 @@ def test_block_local_shift_is_the_running_max_of_block_rules():
                 assert em["m"][b, h, i] == np.float32(m), (b, h, i)
                 assert em["branch"][b, h, i] == br, (b, h, i)
     assert (em["branch"] != 0).sum() > 0
+
+
+def test_compensated_row_sum_keeps_the_blocks_an_fp32_sum_drops():
+    # ijyty.com §7.2 (Kahan summation of the softmax denominator).  Each row sees one score 0
+    # (its unique maximum: P~ = 1) and N - 1 scores whose exp is ~2^-32, so after the first
+    # block every block adds less than half an FP32 ulp of l.  The plain FP32 recurrence
+    # drops all of them; the compensated one keeps them.  The closed form of the LSE is
+    # log(1 + (N - 1) exp(scale * tail)), and the one-shot FP64 oracle reaches it.
+    N = 4096
+    w = inputs.tiny_tail_rows(N=N)
+    q = w.q
+    exact = np.log1p((N - 1) * np.exp(w.scale * -178.0))
+    ref = A.forward(q, w.k, w.v, w.scale, False)
+    np.testing.assert_allclose(ref["lse"], exact, rtol=0, atol=1e-15)
+    plain = E.blocked_forward(q, w.k, w.v, w.scale, False, block_n=128, compensated=False)
+    kahan = E.blocked_forward(q, w.k, w.v, w.scale, False, block_n=128, compensated=True)
+    tail = np.exp(w.scale * -178.0)
+    lost = (N // 128 - 1) * 128 * tail                        # every block after the first
+    assert np.all(np.abs(plain["lse"] - exact) > 0.9 * lost)
+    # compensated: only the first block's own tiny terms (summed with the 1.0 inside the
+    # block) and the FP32 rounding of the final l (half an ulp of 1) remain
+    assert np.all(np.abs(kahan["lse"] - exact) <= 128 * tail + 2.0 ** -24)
+    assert 128 * tail + 2.0 ** -24 < 0.15 * lost
+
+
+def test_compensation_changes_nothing_when_no_block_is_dropped():
+    # on ordinary rows the two recurrences agree to FP32 rounding
+    w = inputs.gpt2_small(B=1, H=1, N=512)
+    a = E.blocked_forward(w.q, w.k, w.v, w.scale, True, stable=1, compensated=False)
+    b = E.blocked_forward(w.q, w.k, w.v, w.scale, True, stable=1, compensated=True)
+    np.testing.assert_allclose(a["lse"], b["lse"], rtol=0, atol=2e-6)
+    np.testing.assert_array_equal(a["ones"], b["ones"])

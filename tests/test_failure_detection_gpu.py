@@ -35,6 +35,10 @@ def hooks_lib():
     lib.fa_bwd.restype = ci
     lib.fa_device_status.argtypes = [vp]
     lib.fa_device_status.restype = ci
+    lib.fa_bwd_noalloc.argtypes = [vp] * 10 + [ci, ci, ci, ci, ci, cf, vp]
+    lib.fa_bwd_noalloc.restype = ci
+    lib.fa_bwd_noalloc_status.argtypes = [vp, ctypes.POINTER(binding.DeviceReport)]
+    lib.fa_bwd_noalloc_status.restype = ci
     lib.fa_last_error.restype = ctypes.c_char_p
     return lib
 
@@ -91,6 +95,39 @@ def test_backward_wait_that_runs_out_reports_timeout_and_context_stays_usable(ho
     monkeypatch.setenv("FA_TEST_INJECT_STALL", "0")
     assert bwd() == binding.FA_OK
     assert hooks_lib.fa_device_status(stream) == binding.FA_OK
+    f = A.forward(w.q, w.k, w.v, w.scale, w.causal)
+    g = A.backward(w.q, w.k, w.v, f["o"], f["lse"], w.do, w.scale, w.causal)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert_close_bf16(name, got, g[name])
+
+
+def test_noalloc_backward_timeout_is_readable_from_its_own_status(hooks_lib, monkeypatch):
+    # fa_bwd_noalloc reports into a static status record of its own: a bounded wait that
+    # runs out there is returned by fa_bwd_noalloc_status (and not by fa_device_status),
+    # the read clears it, and the same context then computes correct gradients
+    w = inputs.gpt2_small(B=1, H=4, N=512)
+    q, k, v, do = to_dev(w)
+    o, lse = binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=1)
+    binding.device_status()
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def bwd():
+        return hooks_lib.fa_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                        do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), None, B, H, N,
+                                        d, int(w.causal), w.scale, stream)
+
+    monkeypatch.setenv("FA_TEST_INJECT_STALL", "1")
+    assert bwd() == binding.FA_OK
+    rep = binding.DeviceReport()
+    assert hooks_lib.fa_bwd_noalloc_status(stream, ctypes.byref(rep)) == binding.FA_ERR_TIMEOUT
+    assert rep.flags & binding.FA_DEVFLAG_TIMEOUT
+    assert hooks_lib.fa_device_status(stream) == binding.FA_OK
+    assert hooks_lib.fa_bwd_noalloc_status(stream, None) == binding.FA_OK
+    monkeypatch.setenv("FA_TEST_INJECT_STALL", "0")
+    assert bwd() == binding.FA_OK
+    assert hooks_lib.fa_bwd_noalloc_status(stream, None) == binding.FA_OK
     f = A.forward(w.q, w.k, w.v, w.scale, w.causal)
     g = A.backward(w.q, w.k, w.v, f["o"], f["lse"], w.do, w.scale, w.causal)
     for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):

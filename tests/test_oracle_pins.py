@@ -240,6 +240,16 @@ def test_near_tie_is_undecidable():
     assert not dec[1]
 
 
+def test_decidability_is_per_row_whatever_the_row_block():
+    # the row blocking only bounds memory: one row at a time gives the same decisions
+    w = inputs.gpt2_medium_sink(B=1, H=1, N=512)
+    for causal in (True, False):
+        d1, b1 = A.decidable_rows(w.q, w.k, causal, 0, 0, row_block=1)
+        d2, b2 = A.decidable_rows(w.q, w.k, causal, 0, 0, row_block=200)
+        np.testing.assert_array_equal(d1, d2)
+        np.testing.assert_array_equal(b1, b2)
+
+
 def test_row_minimum_over_visible_keys():
     # hand example: row 2 sees keys 0..2 (causal) with scores 3, -4, 7 -> min -4
     q = np.array([[[[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]]]])

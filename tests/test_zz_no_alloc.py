@@ -33,7 +33,9 @@ def _grads_both_ways(w):
            torch.empty(q.shape[:3], device=q.device, dtype=torch.float32)]
     rc = binding.fa_bwd_noalloc(q, k, v, o, lse, do, *got, w.causal, w.scale)
     assert rc == binding.FA_OK, binding.last_error()
-    torch.cuda.synchronize()
+    # its kernels report into the entry point's own status record (no timeout, no NaN)
+    rc, rep = binding.fa_bwd_noalloc_status()
+    assert rc == binding.FA_OK and rep["flags"] == 0, (binding.last_error(), rep)
     binding.device_status()
     return ref, got
 
@@ -58,3 +60,26 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = binding.fa_bwd_noalloc(x, x, x, x, lse, x, x, x, x, None, True, 0.088)
     assert rc == binding.FA_ERR_INVALID_ARG
     assert "fa_bwd_noalloc holds at most" in binding.last_error()
+
+
+def test_noalloc_status_reports_nonfinite_gradients_and_clears():
+    # A NaN in dO reaches dQ, dK and dV.  The no-allocation entry point's own status record
+    # reports it (with per-output counts equal to the non-finite entries written), a second
+    # read finds it clear, and the library's allocated record is not touched.
+    w = inputs.random_case(1, 2, 256, 64, True, seed=4)
+    q, k, v, do = to_dev(w)
+    o, lse = binding.forward(q, k, v, causal=True, scale=w.scale)
+    binding.device_status()
+    do[0, 0, 200, 5] = float("nan")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    assert binding.fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, None, True, w.scale) == binding.FA_OK
+    rc, rep = binding.fa_bwd_noalloc_status()
+    assert rc == binding.FA_WARN_NONFINITE
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert rep["nonfinite"][name] == int((~torch.isfinite(t.float())).sum().item()) > 0, (name, rep)
+    assert rep["nonfinite"]["o"] == rep["nonfinite"]["lse"] == 0
+    assert binding.fa_bwd_noalloc_status()[0] == binding.FA_OK
+    assert binding.fa_device_report_read()[0] == binding.FA_OK
+    do[0, 0, 200, 5] = 0.0
+    assert binding.fa_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, None, True, w.scale) == binding.FA_OK
+    assert binding.fa_bwd_noalloc_status()[0] == binding.FA_OK
