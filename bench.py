@@ -460,10 +460,12 @@ def run_native(args):
 
 # --------------------------------------------------------------------------- profiling case
 def run_profile_case(args):
-    """One launch of each kernel on an 8-head slice of the 8k-token workload, for ncu.
+    """One launch of each kernel on a small case, for ncu.
 
-    The slice keeps every input larger than the L2 (Q, K, V, dO 16.8 MB each, the FP32 dQ
-    accumulator 33.6 MB) with well under 1 GB on the device, so a capture ends in minutes.
+    llama7b_8heads (default): an 8-head slice of the 8k-token workload; every input stays
+    larger than the L2 (Q, K, V, dO 16.8 MB each, the FP32 dQ accumulator 33.6 MB) with well
+    under 1 GB on the device, so a capture ends in minutes.  gpt2_small: the whole GPT-2-small
+    workload (d = 64; its inputs fit in the L2).
     Order: BF16 forward, backward (preprocess, main, dQ convert), FP8 quantise x3, FP8 forward.
     """
     import torch
@@ -471,10 +473,13 @@ def run_profile_case(args):
     from numerics_tcgen05_tmem_gb300 import binding, build, inputs
 
     build.build()
-    w = inputs.llama7b_long(heads=list(range(8)))
+    if args.profile_case == "gpt2_small":
+        w = inputs.gpt2_small()
+    else:
+        w = inputs.llama7b_long(heads=list(range(8)))
     q, k, v, do = (t.to("cuda") for t in (w.q, w.k, w.v, w.do))
-    o, lse = binding.forward(q, k, v, causal=True, scale=w.scale, stable=1, beta=w.beta)
-    binding.backward(q, k, v, o, lse, do, causal=True, scale=w.scale)
+    o, lse = binding.forward(q, k, v, causal=w.causal, scale=w.scale, stable=1, beta=w.beta)
+    binding.backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale)
     (q8, dq), (k8, dk), (v8, dv) = (binding.quantize_fp8(t) for t in (q, k, v))
     binding.forward_fp8(q8, k8, v8, torch.cat([dq, dk, dv]), causal=True, scale=w.scale, stable=1, beta=w.beta)
     binding.device_status()
@@ -667,8 +672,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload block of the bench line")
     ap.add_argument("--configs", action="store_true",
                     help="time forward and backward of every workload (one JSON line each) and exit")
-    ap.add_argument("--profile-case", action="store_true",
-                    help="run each kernel once on an 8-head slice (for ncu captures) and exit")
+    ap.add_argument("--profile-case", nargs="?", const="llama7b_8heads", choices=("llama7b_8heads", "gpt2_small"),
+                    help="run each kernel once on a small case (for ncu captures) and exit")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
