@@ -44,25 +44,44 @@ namespace fwd {
 
 constexpr int kBlockM = 128;   // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;   // keys per block
-constexpr int kTiles = 2;      // query tiles per CTA
-constexpr int kThreads = 512;  // 16 warps
-constexpr int kMmaWarp = 12;
-constexpr int kLoadWarp = 13;  // warps 14-15 only take part in set-up and teardown
 constexpr int kPScaleLog2 = 8;  // FP8 path: P~ is scaled by 2^8 before its E4M3 rounding
-// Per-thread register budgets after the launch (setmaxnreg); the launch gives every thread
-// kRegLaunch registers and the split below must not exceed 512 * kRegLaunch.
-constexpr int kRegLaunch = 128;
-constexpr int kRegSoftmax = 176, kRegCorr = 96, kRegOther = 56;
-static_assert(2 * 128 * kRegSoftmax + 128 * kRegCorr + 128 * kRegOther <= kThreads * kRegLaunch,
-              "register split exceeds the launch allocation");
+
+// CTA shape for kT query tiles of 128 rows.
+//   kT = 2: warps 0-7 softmax (one warpgroup per tile), 8-11 correction, 12 MMA, 13 TMA,
+//           14-15 set-up and teardown only; 512 threads, all 512 TMEM columns, one CTA per SM.
+//   kT = 1: warps 0-3 softmax, 4-7 correction, 8 MMA, 9 TMA, 10-11 set-up and teardown only;
+//           384 threads, 256 TMEM columns and under 100 KB of shared memory at d = 64, so two
+//           CTAs share an SM and one's pipeline fill and drain overlap the other's work (short
+//           rows, small grids).
+// setmaxnreg acts on whole warpgroups, hence the idle warps that complete the last one.
+// Registers are rebalanced after the launch (setmaxnreg): softmax threads hold a whole
+// 128-column row of S, the others need few; the split must not exceed the launch allocation.
+template <int kT>
+struct Shape {
+  static constexpr int kTiles = kT;
+  static constexpr int kSoftmaxWarps = 4 * kT;
+  static constexpr int kMmaWarp = 4 * kT + 4;
+  static constexpr int kLoadWarp = 4 * kT + 5;
+  static constexpr int kThreads = (kT == 2) ? 512 : 384;
+  static constexpr int kCtasPerSm = (kT == 2) ? 1 : 2;
+  static constexpr uint32_t kTmemCols = (kT == 2) ? 512 : 256;
+  static constexpr int kRegLaunch = (kT == 2) ? 128 : 80;
+  static constexpr int kRegSoftmax = (kT == 2) ? 176 : 168, kRegCorr = (kT == 2) ? 96 : 40,
+                       kRegOther = (kT == 2) ? 56 : 32;
+  static constexpr int kSplit = 128 * kT * kRegSoftmax + 128 * kRegCorr + (kThreads - 128 * kT - 128) * kRegOther;
+  static_assert(kSplit <= kThreads * kRegLaunch, "register split exceeds the launch allocation");
+  static_assert(kRegLaunch * kThreads * kCtasPerSm <= 65536, "launch registers exceed the SM's file");
+};
 
 // kFp8: Q, K, V (and P~ for the P~V product) are E4M3 instead of BF16.  Every operand row
 // is then D bytes, so a 128-byte swizzle atom spans 128 elements instead of 64, and one MMA
 // instruction consumes 32 elements of K instead of 16 -- always 32 bytes per k-step.
-template <int D, bool kFp8 = false>
+template <int D, bool kFp8 = false, int kT = 2>
 struct Cfg {
+  static constexpr int kTiles = kT;
   static constexpr int kElem = kFp8 ? 1 : 2;                // bytes per Q/K/V element
-  static constexpr int kStages = kFp8 ? 4 : ((D == 128) ? 2 : 4);
+  // K/V ring depth: what fits beside the Q tiles (two CTAs per SM for kT = 1)
+  static constexpr int kStages = kFp8 ? 4 : ((kT == 1 || D == 128) ? 2 : 4);
   static constexpr int kTileBytes = kBlockM * D * kElem;    // one 128 x D tile (Q, K or V)
   // Swizzle atom: 128-byte rows, or 64-byte rows when a tile row is only 64 bytes (E4M3, d = 64)
   static constexpr int kAtomBytes = (D * kElem >= 128) ? 128 : 64;
@@ -77,12 +96,12 @@ struct Cfg {
   static constexpr int kKOff = kQOff + kTiles * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kVOff + kStages * kTileBytes + 1024;  // +1024 for alignment
-  // d = 64 leaves 128 TMEM columns beside S0 | S1 | O0 | O1: a third S buffer.  The S of
-  // (tile t, block j) then goes to buffer (2j + t) mod 3, so a tile's next S can be computed
-  // while its softmax still works on the current one.
-  static constexpr bool kRing = (D == 64);
+  // d = 64 with two tiles leaves 128 TMEM columns beside S0 | S1 | O0 | O1: a third S
+  // buffer.  The S of (tile t, block j) then goes to buffer (2j + t) mod 3, so a tile's next S
+  // can be computed while its softmax still works on the current one.  One tile: S0 | O0.
+  static constexpr bool kRing = (D == 64 && kT == 2);
   static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
-  static constexpr uint32_t kTmemO0 = kRing ? 384 : 256, kTmemO1 = kTmemO0 + D;
+  static constexpr uint32_t kTmemO0 = kRing ? 384 : 128 * kT, kTmemO1 = kTmemO0 + D;
   __device__ static uint32_t s_col(int t, int j) {
     return kRing ? (uint32_t)(((2 * j + t) % 3) * 128) : (t == 0 ? kTmemS0 : kTmemS1);
   }
@@ -90,7 +109,9 @@ struct Cfg {
   static constexpr uint32_t kIdescS = kFp8 ? idesc_e4m3(128, kBlockN, false, false) : idesc_bf16(128, kBlockN, false, false);
   static constexpr uint32_t kIdescO = kFp8 ? idesc_e4m3(128, D, false, true) : idesc_bf16(128, D, false, true);
   static_assert(kAtoms >= 1 && kAtoms * kAtomBytes == D * kElem, "tile rows must be whole swizzle atoms");
-  static_assert((kRing ? 3 : 2) * 128 <= kTmemO0 && kTmemO1 + D <= 512, "TMEM plan exceeds 512 columns");
+  static_assert((kRing ? 3 : kT) * 128 <= kTmemO0 && kTmemO0 + kT * D <= Shape<kT>::kTmemCols,
+                "TMEM plan exceeds the allocation");
+  static_assert(kT == 2 || 2 * (kSmemBytes + 4096) <= 228 * 1024, "two CTAs must fit one SM's shared memory");
   // shared-memory descriptor of an operand in this tile layout (8-row groups kAtomBytes * 8 apart)
   __device__ static uint64_t sdesc(uint32_t saddr, uint32_t lbo) {
     return kAtomBytes == 128 ? sdesc_sw128(saddr, lbo, 8 * kAtomBytes) : sdesc_sw64(saddr, lbo, 8 * kAtomBytes);
@@ -115,7 +136,7 @@ struct Params {
   DevStatus* status;
   int N;
   int BH;
-  int n_qblocks;   // ceil(N / 256)
+  int n_qblocks;   // ceil(N / (128 kT))
   int causal;
   float scale;
   float scale_log2;  // scale * log2(e)
@@ -124,6 +145,7 @@ struct Params {
   int inject_stall;  // test builds only (FA_TEST_HOOKS): make the MMA warp's first wait run out
 };
 
+template <int kTiles>
 struct Shared {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
@@ -151,8 +173,9 @@ struct Shared {
   uint32_t abort_flag;
 };
 
-// Which key blocks tile t of query block qb attends: [0, nb).  0 if the tile is
-// entirely past N.
+// Which key blocks tile t of query block qb (kTiles tiles of 128 rows) attends: [0, nb).
+// 0 if the tile is entirely past N.
+template <int kTiles>
 __device__ __forceinline__ int tile_blocks(const Params& p, int qb, int t) {
   const int row0 = qb * (kTiles * kBlockM) + t * kBlockM;
   if (row0 >= p.N) return 0;
@@ -165,21 +188,23 @@ __device__ __forceinline__ int tile_blocks(const Params& p, int qb, int t) {
 // kStable: 0 = plain shift (running max); 1 = stabilised shift on the running (max, count)
 // of the row; 2 = block-local reading: each key block's own (max, count) picks a shift by
 // the same rule and the row keeps the largest shift seen so far.
-template <int D, int kStable, bool kStats, bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int kStable, bool kStats, bool kFp8, int kT>
+__global__ void __launch_bounds__(Shape<kT>::kThreads, Shape<kT>::kCtasPerSm)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using C = Cfg<D, kFp8>;
+  using C = Cfg<D, kFp8, kT>;
+  using L = Shape<kT>;
+  constexpr int kTiles = kT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ Shared sh;
+  __shared__ Shared<kT> sh;
   volatile uint32_t* abort_flag = &sh.abort_flag;
 
   const int warp = threadIdx.x / 32;
   // heaviest (largest causal) query blocks first
   const int qb = p.causal ? (p.n_qblocks - 1 - (int)(blockIdx.x / p.BH)) : (int)(blockIdx.x / p.BH);
   const int bh = blockIdx.x % p.BH;
-  const int nb0 = tile_blocks(p, qb, 0), nb1 = tile_blocks(p, qb, 1);
+  const int nb0 = tile_blocks<kT>(p, qb, 0), nb1 = (kT > 1) ? tile_blocks<kT>(p, qb, 1) : 0;
   const int nbmax = max(nb0, nb1);
 
   if (threadIdx.x == 0) {
@@ -210,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     FA_BOUNDS_OK((uint32_t)(smem - smem_raw) + C::kVOff + C::kStages * C::kTileBytes <= dynamic_smem_bytes(),
                  p.status, kSiteFwdSmemSize, dynamic_smem_bytes());
   }
-  if (warp == kMmaWarp) {
-    tmem_alloc(&sh.tmem_base, 512);
+  if (warp == L::kMmaWarp) {
+    tmem_alloc(&sh.tmem_base, L::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -220,15 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sh.tmem_base;
   // Roles by warpgroup; each branch first rebalances its registers (setmaxnreg) so the
   // softmax warpgroups can hold a 128-column row of S each.
-  if (warp >= 12) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegOther));
-  if (warp == kLoadWarp) {
+  if (warp >= L::kMmaWarp) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kRegOther));
+  if (warp == L::kLoadWarp) {
     // ------------------------------------------------------------ TMA producer
     if (elect_one()) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      const int ntiles = (nb1 > 0) ? 2 : 1;
+      const int ntiles = (kT > 1 && nb1 > 0) ? 2 : 1;
       mbar_arrive_expect_tx(&sh.q_full, ntiles * C::kTileBytes);
       for (int t = 0; t < ntiles; ++t)
         if (FA_BOUNDS_OK(qb * (kTiles * kBlockM) + t * kBlockM < p.N, p.status, kSiteFwdQRow,
@@ -264,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&sh.v_full[j % C::kStages], (j / C::kStages) & 1, &ignore_abort, p.status);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == L::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       const uint32_t sQ = smem_u32(smem + C::kQOff);
@@ -411,9 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  } else if (warp < 8) {
+  } else if (warp < L::kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax warpgroups
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(L::kRegSoftmax));
     const int t = warp / 4;                      // tile
     const int lane_base = (warp % 4) * 32;       // TMEM lane quarter of this warp
     const int r = lane_base + (threadIdx.x % 32);  // row within the tile
@@ -661,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ correction warpgroup
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegCorr));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(L::kRegCorr));
     // O_t <- alpha O_t between P~V products (ijyty.com §2.1, O = diag(exp(m_prev - m)) O_prev + P~V),
     // then the epilogue O = O / l.  Thread = row of the lane quarter, for both tiles.
     const int lane_base = (warp % 4) * 32;
@@ -741,9 +766,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == L::kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, L::kTmemCols);
   }
 }
 
@@ -752,11 +777,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 namespace {
 
-template <int D, int kStable, bool kStats, bool kFp8>
-int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::fwd::Params& p,
+template <int D, int kStable, bool kStats, bool kFp8, int kT>
+int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const fa::fwd::Params& p0,
                cudaStream_t stream) {
-  using C = fa::fwd::Cfg<D, kFp8>;
-  auto kern = fa::fwd::fa_fwd_kernel<D, kStable, kStats, kFp8>;
+  using C = fa::fwd::Cfg<D, kFp8, kT>;
+  using L = fa::fwd::Shape<kT>;
+  auto kern = fa::fwd::fa_fwd_kernel<D, kStable, kStats, kFp8, kT>;
+  fa::fwd::Params p = p0;
+  p.n_qblocks = (p.N + kT * fa::fwd::kBlockM - 1) / (kT * fa::fwd::kBlockM);
   int rc = fa::check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
                           "cudaFuncSetAttribute(fwd)");
   if (rc) return rc;
@@ -764,23 +792,39 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   // to launch a build whose launch allocation is smaller than the split needs
   cudaFuncAttributes attr;
   if ((rc = fa::check_cuda(cudaFuncGetAttributes(&attr, kern), "cudaFuncGetAttributes(fwd)"))) return rc;
-  constexpr int kSplit = 2 * 128 * fa::fwd::kRegSoftmax + 128 * fa::fwd::kRegCorr + 128 * fa::fwd::kRegOther;
-  if (attr.numRegs * fa::fwd::kThreads < kSplit)
+  if (attr.numRegs * L::kThreads < L::kSplit)
     return fa::set_error(FA_ERR_CUDA, "forward kernel built with %d registers/thread; its register split needs %d",
-                         attr.numRegs, (kSplit + fa::fwd::kThreads - 1) / fa::fwd::kThreads);
+                         attr.numRegs, (L::kSplit + L::kThreads - 1) / L::kThreads);
   const dim3 grid((unsigned)(p.n_qblocks * p.BH));
-  kern<<<grid, fa::fwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  kern<<<grid, L::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return fa::check_cuda(cudaGetLastError(), "launch fa_fwd_kernel");
 }
+
+template <int D, bool kFp8, int kT>
+int dispatch_fwd_tiles(int stable, bool stats, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const fa::fwd::Params& p, cudaStream_t s) {
+  if (stable == 2)
+    return stats ? launch_fwd<D, 2, true, kFp8, kT>(tq, tk, tv, p, s) : launch_fwd<D, 2, false, kFp8, kT>(tq, tk, tv, p, s);
+  if (stable == 1)
+    return stats ? launch_fwd<D, 1, true, kFp8, kT>(tq, tk, tv, p, s) : launch_fwd<D, 1, false, kFp8, kT>(tq, tk, tv, p, s);
+  return stats ? launch_fwd<D, 0, true, kFp8, kT>(tq, tk, tv, p, s) : launch_fwd<D, 0, false, kFp8, kT>(tq, tk, tv, p, s);
+}
+
+// At d = 64 and up to kShortRows keys, one query tile per CTA with two CTAs per SM: rows of
+// at most 16 key blocks spend much of a CTA's life filling and draining its pipeline, and a
+// second CTA on the SM covers that (GPT-2-shaped problems, 1024 tokens: +5-13 %).  Longer rows
+// keep two tiles per CTA, whose third S buffer in TMEM is worth more there (16k tokens: the
+// single-tile CTA is 5-12 % slower).  d = 128 always takes two tiles (two CTAs' shared memory
+// would not fit an SM).
+constexpr int kShortRows = 2048;
 
 template <int D, bool kFp8>
 int dispatch_fwd(int stable, bool stats, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                  const fa::fwd::Params& p, cudaStream_t s) {
-  if (stable == 2)
-    return stats ? launch_fwd<D, 2, true, kFp8>(tq, tk, tv, p, s) : launch_fwd<D, 2, false, kFp8>(tq, tk, tv, p, s);
-  if (stable == 1)
-    return stats ? launch_fwd<D, 1, true, kFp8>(tq, tk, tv, p, s) : launch_fwd<D, 1, false, kFp8>(tq, tk, tv, p, s);
-  return stats ? launch_fwd<D, 0, true, kFp8>(tq, tk, tv, p, s) : launch_fwd<D, 0, false, kFp8>(tq, tk, tv, p, s);
+  if constexpr (D == 64) {
+    if (p.N <= kShortRows) return dispatch_fwd_tiles<D, kFp8, 1>(stable, stats, tq, tk, tv, p, s);
+  }
+  return dispatch_fwd_tiles<D, kFp8, 2>(stable, stats, tq, tk, tv, p, s);
 }
 
 // Argument checks and kernel parameters shared by the BF16 and FP8 entry points.
@@ -812,7 +856,6 @@ int prepare_fwd(fa::fwd::Params& p, bool& want_stats, const void* q, const void*
   if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
   p.N = N;
   p.BH = B * H;
-  p.n_qblocks = (N + fwd::kTiles * fwd::kBlockM - 1) / (fwd::kTiles * fwd::kBlockM);
   p.causal = causal ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -92,13 +92,14 @@ def test_quantize_full_size_tensors():
 
 # ----------------------------------------------------------------- forward
 
-@pytest.mark.parametrize("N", [300, 2048])
+@pytest.mark.parametrize("N", [300, 2048, 2560])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("stable", [0, 1, 2])
 def test_tiny_ties_exact_statistics(stable, d, N):
     # k/8 with |k| <= 16 is exact in E4M3 and the dot products are exact in FP32, so with
     # unit scales the row maximum, ties, branch and the exact-1.0 counts are decidable
-    # (N = 2048: 16 key blocks, with ties first reached late in the row)
+    # (N = 2048: 16 key blocks, with ties first reached late in the row; at d = 64 rows of up
+    # to 2048 keys run one query tile per CTA, longer ones two)
     w = inputs.tiny_ties(d=d, N=N, H=2)
     vals = [t.double().numpy() for t in (w.q, w.k, w.v)]
     codes = [F.encode_e4m3(x) for x in vals]

@@ -96,6 +96,28 @@ def test_full_length_dyadic_rows_exact_statistics(stable):
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
 
 
+@pytest.mark.parametrize("N", [2048, 2049, 4096])
+@pytest.mark.parametrize("stable", [0, 1, 2])
+def test_d64_both_cta_shapes_exact_statistics(N, stable):
+    # At d = 64 the forward runs one query tile per CTA (two CTAs per SM) for rows of up to
+    # 2048 keys and two tiles per CTA (with a third S buffer) beyond: both shapes must give
+    # the oracle's statistics bit for bit on exact (dyadic) scores, causal and not.
+    for causal in (True, False):
+        w0 = inputs.tiny_ties(N=N, H=2, d=64)
+        w = inputs.Workload(w0.name, w0.q, w0.k, w0.v, w0.do, causal, w0.scale, stable, w0.beta)
+        o, lse, st = run_fwd(w, stable)
+        ref = A.forward(w.q, w.k, w.v, w.scale, causal, stable=1 if stable == 2 else stable, beta=w.beta)
+        em = E.blocked_forward(w.q, w.k, w.v, w.scale, causal, stable=stable, beta=w.beta, block_n=128)
+        assert_close_bf16("o", o, ref["o"])
+        assert_lse(lse, ref["lse"])
+        np.testing.assert_array_equal(st["row_max_raw"].cpu().numpy().astype(np.float64), ref["rm"])
+        np.testing.assert_array_equal(st["row_ties"].cpu().numpy(), ref["rs"])
+        np.testing.assert_array_equal(st["row_branch"].cpu().numpy(), em["branch"])
+        np.testing.assert_array_equal(st["row_ones"].cpu().numpy(), em["ones"])
+        o2, lse2 = run_fwd(w, stable, stats=False)
+        assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
 @pytest.mark.parametrize("stable", [0, 1])
 def test_gpt2_small_full(stable):
     w = inputs.gpt2_small()
