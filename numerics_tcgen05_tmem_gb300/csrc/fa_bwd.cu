@@ -646,17 +646,13 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   p.inject_stall = (inject && inject[0] == '1') ? 1 : 0;
 #endif
   auto kern = bwd::fa_bwd_main<D>;
-  if ((rc = check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
-                       "cudaFuncSetAttribute(bwd)")))
-    return rc;
   // setmaxnreg.inc waits until the block's launch registers cover the new split: refuse to
   // launch a build whose launch allocation is smaller than the split needs
-  cudaFuncAttributes attr;
-  if ((rc = check_cuda(cudaFuncGetAttributes(&attr, kern), "cudaFuncGetAttributes(bwd)"))) return rc;
   constexpr int kSplit = 2 * 128 * bwd::kRegPdS + 128 * bwd::kRegDQ + 128 * bwd::kRegOther;
-  if (attr.numRegs * bwd::kThreads < kSplit)
-    return set_error(FA_ERR_CUDA, "backward kernel built with %d registers/thread; its register split needs %d",
-                     attr.numRegs, (kSplit + bwd::kThreads - 1) / bwd::kThreads);
+  static std::atomic<uint64_t> prepared{0};
+  if ((rc = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, bwd::kThreads, kSplit,
+                           "backward kernel", &prepared)))
+    return rc;
   kern<<<(unsigned)(p.n_tiles * p.BH), bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
   if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_main"))) return rc;
   }

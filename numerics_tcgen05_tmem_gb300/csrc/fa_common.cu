@@ -91,6 +91,25 @@ int sm_count() {
   return g_sms[dev];
 }
 
+int prepare_kernel(const void* kern, int smem_bytes, int threads, int split, const char* name,
+                   std::atomic<uint64_t>* done) {
+  int dev = 0;
+  int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done->load(std::memory_order_acquire) & bit)) return FA_OK;
+  if ((rc = check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes),
+                       "cudaFuncSetAttribute")))
+    return rc;
+  cudaFuncAttributes attr;
+  if ((rc = check_cuda(cudaFuncGetAttributes(&attr, kern), "cudaFuncGetAttributes"))) return rc;
+  if (attr.numRegs * threads < split)
+    return set_error(FA_ERR_CUDA, "%s built with %d registers/thread; its register split needs %d", name,
+                     attr.numRegs, (split + threads - 1) / threads);
+  if (bit) done->fetch_or(bit, std::memory_order_acq_rel);
+  return FA_OK;
+}
+
 static int encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, int elem_bytes, const void* base, int BH, int N,
                      int d, int box_cols, int box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   {

@@ -785,16 +785,12 @@ int launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& 
   auto kern = fa::fwd::fa_fwd_kernel<D, kStable, kStats, kFp8, kT>;
   fa::fwd::Params p = p0;
   p.n_qblocks = (p.N + kT * fa::fwd::kBlockM - 1) / (kT * fa::fwd::kBlockM);
-  int rc = fa::check_cuda(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes),
-                          "cudaFuncSetAttribute(fwd)");
-  if (rc) return rc;
   // setmaxnreg.inc waits until the block's launch registers can cover the new split: refuse
   // to launch a build whose launch allocation is smaller than the split needs
-  cudaFuncAttributes attr;
-  if ((rc = fa::check_cuda(cudaFuncGetAttributes(&attr, kern), "cudaFuncGetAttributes(fwd)"))) return rc;
-  if (attr.numRegs * L::kThreads < L::kSplit)
-    return fa::set_error(FA_ERR_CUDA, "forward kernel built with %d registers/thread; its register split needs %d",
-                         attr.numRegs, (L::kSplit + L::kThreads - 1) / L::kThreads);
+  static std::atomic<uint64_t> prepared{0};
+  int rc = fa::prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, L::kThreads, L::kSplit,
+                              "forward kernel", &prepared);
+  if (rc) return rc;
   const dim3 grid((unsigned)(p.n_qblocks * p.BH));
   kern<<<grid, L::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   return fa::check_cuda(cudaGetLastError(), "launch fa_fwd_kernel");

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include <nvtx3/nvToolsExt.h>
 
 #include "../../include/fa.h"
@@ -62,5 +64,13 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// Once per kernel and device: raise the kernel's dynamic shared memory limit to smem_bytes and
+// check that its launch register allocation (registers per thread x threads) covers the
+// setmaxnreg split of `split` registers -- setmaxnreg.inc would otherwise wait forever.  `done`
+// is the kernel's own bit mask of devices already prepared (a static of the caller); later
+// calls on a prepared device cost one cudaGetDevice and an atomic load.
+int prepare_kernel(const void* kern, int smem_bytes, int threads, int split, const char* name,
+                   std::atomic<uint64_t>* done);
 
 }  // namespace fa
