@@ -26,7 +26,8 @@
 //              accumulator through shared-memory staging and TMA reduce-adds.
 //   warp  12   MMA issuer;  warp 13  TMA producer (Q, dO tiles and the per-tile
 //              lse / delta vectors, double-buffered);  warps 14-15 set-up/teardown only.
-// Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV.
+// Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV, and
+// at d = 64 a second S^T buffer in the last 128 columns (S^T of odd query steps).
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdlib.h>
@@ -50,10 +51,15 @@ constexpr int kRegLaunch = 128;
 constexpr int kRegPdS = 144, kRegDQ = 152, kRegOther = 72;
 static_assert(2 * 128 * kRegPdS + 128 * kRegDQ + 128 * kRegOther <= kThreads * kRegLaunch,
               "register split exceeds the launch allocation");
-constexpr int kStages = 2;      // Q-tile ring depth (dO is single-buffered)
+constexpr int kMaxStages = 3;   // deepest Q-tile ring (dO is single-buffered)
 
 template <int D>
 struct Cfg {
+  // d = 64 has room for a third Q stage and a second S^T buffer in TMEM: S_{i+2} is computed
+  // into the other buffer while the P/dS warpgroups still work on step i+1
+  static constexpr int kStages = (D == 64) ? 3 : 2;   // Q-tile ring depth
+  static constexpr bool kDoubleS = (D == 64);
+  static_assert(kStages <= kMaxStages, "Q ring deeper than the barrier arrays");
   static constexpr int kTileBytes = kBlock * D * 2;
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
@@ -70,7 +76,13 @@ struct Cfg {
   static constexpr int kBarOff = kDeltaOff + kStages * kBlock * 4;
   static constexpr int kSmemBytes = kBarOff + 256;
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 128, kTmemDK = 256, kTmemDV = 256 + D;
-  static_assert(kTmemDV + D <= 512 && kTmemDQ + D <= kTmemDK, "TMEM plan exceeds 512 columns");
+  static constexpr uint32_t kTmemS1 = kTmemDV + D;  // second S^T buffer (d = 64)
+  static_assert(kTmemDV + D <= 512 && kTmemDQ + D <= kTmemDK && (!kDoubleS || kTmemS1 + 128 <= 512),
+                "TMEM plan exceeds 512 columns");
+  // S^T (then P^T) of query step `it`, and the barrier slot / parity of its s_full event
+  __device__ static uint32_t s_col(int it) { return (kDoubleS && (it & 1)) ? kTmemS1 : kTmemS; }
+  __device__ static int s_slot(int it) { return kDoubleS ? (it & 1) : 0; }
+  __device__ static uint32_t s_parity(int it) { return kDoubleS ? (uint32_t)((it >> 1) & 1) : (uint32_t)(it & 1); }
   static constexpr uint32_t kIdescSq = idesc_bf16(128, kBlock, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescKV = idesc_bf16(128, D, false, true);        // dV (TMEM A), dK
   static constexpr uint32_t kIdescQ = idesc_bf16(128, D, true, true);          // dQ: A = dS (MN-major)
@@ -78,8 +90,8 @@ struct Cfg {
 
 struct Bars {
   uint64_t kv_full;
-  uint64_t q_full[kStages], q_empty[kStages], do_full, do_empty;
-  uint64_t s_full, p_ready, dp_full, ds_ready, ds_empty, dq_full, dq_empty, mma_done;
+  uint64_t q_full[kMaxStages], q_empty[kMaxStages], do_full, do_empty;
+  uint64_t s_full[2], p_ready, dp_full, ds_ready, ds_empty, dq_full, dq_empty, mma_done;
   uint64_t never;  // test builds only: a barrier nothing arrives on
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -197,13 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     sh.abort_flag = 0;
     mbar_init(&sh.kv_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sh.q_full[s], 1);
       mbar_init(&sh.q_empty[s], 1);
     }
     mbar_init(&sh.do_full, 1);
     mbar_init(&sh.do_empty, 1);
-    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.s_full[0], 1);
+    mbar_init(&sh.s_full[1], 1);
     mbar_init(&sh.p_ready, 2 * kBlock);
     mbar_init(&sh.dp_full, 1);
     mbar_init(&sh.ds_ready, 2 * kBlock);
@@ -242,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t stat_base = (size_t)bh * p.N_pad;
       int nq = 0, ndo = 0;
       for (int it = 0; it < n_it; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
+        const int s = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
         const int row0 = (i0 + it) * kBlock;
         if (!mbar_wait(&sh.q_empty[s], ph ^ 1, abort_flag, p.status)) break;
         if (!FA_BOUNDS_OK(row0 < p.N_pad && (long long)stat_base + row0 + kBlock <= (long long)p.BH * p.N_pad,
@@ -266,8 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // let copies still in flight land before the CTA's shared memory goes away
         volatile uint32_t ignore_abort = 0;
         mbar_wait(&sh.kv_full, 0, &ignore_abort, p.status);
-        for (int it = max(0, nq - kStages); it < nq; ++it)
-          mbar_wait(&sh.q_full[it % kStages], (it / kStages) & 1, &ignore_abort, p.status);
+        for (int it = max(0, nq - C::kStages); it < nq; ++it)
+          mbar_wait(&sh.q_full[it % C::kStages], (it / C::kStages) & 1, &ignore_abort, p.status);
         if (ndo > 0) mbar_wait(&sh.do_full, (ndo - 1) & 1, &ignore_abort, p.status);
       }
     }
@@ -288,13 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.inject_stall) ok = ok && mbar_wait(&sh.never, 0, abort_flag, p.status);
 #endif
       auto issue_s = [&](int it) {  // S^T = K_j Q_i^T
-        const int s = it % kStages;
-        if (!(ok = mbar_wait(&sh.q_full[s], (it / kStages) & 1, abort_flag, p.status))) return;
+        const int s = it % C::kStages;
+        if (!(ok = mbar_wait(&sh.q_full[s], (it / C::kStages) & 1, abort_flag, p.status))) return;
         tc_fence_after();
         const uint32_t q = sQ + s * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kTmemS, kmaj(sK, kk), kmaj(q, kk), C::kIdescSq, kk > 0);
-        tc_commit(&sh.s_full);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::s_col(it), kmaj(sK, kk), kmaj(q, kk), C::kIdescSq, kk > 0);
+        tc_commit(&sh.s_full[C::s_slot(it)]);
       };
       const uint32_t dO = sDO;
       // dP^T = V_j dO_i^T into dP^T's columns (which held dQ_{i-1}: wait until drained)
@@ -314,23 +328,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk)
-          mma_ts(tmem + C::kTmemDV, tmem + C::kTmemS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(dO, kk),
+          mma_ts(tmem + C::kTmemDV, tmem + C::s_col(it) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(dO, kk),
                  C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
       };
       // Issue order (same-thread MMAs execute in order):
       //   S_0 dP_0 dV_0 S_1 | dK_0 dQ_0 dP_1 dV_1 S_2 | dK_1 dQ_1 dP_2 dV_2 S_3 | ...
       // dP_{i+1} needs only dO and the drained dQ_i columns, so it runs while the softmax
-      // warpgroups compute P_{i+1}; dV_{i+1} follows once P_{i+1} is in TMEM.
+      // warpgroups compute P_{i+1}; dV_{i+1} follows once P_{i+1} is in TMEM.  With two S^T
+      // buffers (d = 64) S_{i+2} goes before dV_{i+1}: its buffer's last reader, dV_i, was
+      // issued a round earlier.
       if (ok && n_it > 0) {
         tc_fence_after();
         issue_s(0);
         if (ok) issue_dp(0);
+        if (C::kDoubleS && ok && n_it > 1) issue_s(1);
         if (ok) issue_dv(0);
         if (ok) tc_commit(&sh.do_empty);
-        if (ok && n_it > 1) issue_s(1);
+        if (!C::kDoubleS && ok && n_it > 1) issue_s(1);
       }
       for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % kStages;
+        const int s = it % C::kStages;
         const uint32_t q = sQ + s * C::kTileBytes;
         // dK += dS^T Q_i ;  dQ_i = dS K_j
         if (!(ok = mbar_wait(&sh.ds_ready, it & 1, abort_flag, p.status))) break;
@@ -351,10 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it + 1 < n_it) {
           issue_dp(it + 1);
           if (!ok) break;
+          if (C::kDoubleS && it + 2 < n_it) {
+            issue_s(it + 2);
+            if (!ok) break;
+          }
           issue_dv(it + 1);
           if (!ok) break;
           tc_commit(&sh.do_empty);
-          if (it + 2 < n_it) {
+          if (!C::kDoubleS && it + 2 < n_it) {
             issue_s(it + 2);
             if (!ok) break;
           }
@@ -376,19 +397,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane_base = (warp % 4) * 32;
     const int r = lane_base + (threadIdx.x % 32);  // key row within the tile (= TMEM lane)
     const uint32_t lane_off = (uint32_t)lane_base << 16;
-    const uint32_t tS = tmem + C::kTmemS + lane_off + 64 * h;
+    const uint32_t tS0 = tmem + lane_off + 64 * h;  // + the step's S^T buffer column
     const uint32_t tDP = tmem + C::kTmemDP + lane_off + 64 * h;
     const float c = p.scale_log2;
     uint8_t* ds_row = smem + C::kDSOff + h * 16384 + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int s = it % kStages;
+      const int s = it % C::kStages;
       const bool diag = p.causal && it == 0;  // query tile i0 == key tile jt: mask q < key
+      const uint32_t tS = tS0 + C::s_col(it);
       const float4* lse4 = reinterpret_cast<const float4*>(smem + C::kLseOff + s * kBlock * 4) + 16 * h;
       const float4* dl4 = reinterpret_cast<const float4*>(smem + C::kDeltaOff + s * kBlock * 4) + 16 * h;
-      if (!(ok = mbar_wait(&sh.q_full[s], (it / kStages) & 1, abort_flag, p.status))) break;
-      if (!(ok = mbar_wait(&sh.s_full, it & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.q_full[s], (it / C::kStages) & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.s_full[C::s_slot(it)], C::s_parity(it), abort_flag, p.status))) break;
       tc_fence_after();
       // P^T = exp2(S^T c - lse_q log2 e); padded queries carry lse = +inf -> 0
       // this warpgroup's 64 columns of the row in one round trip
@@ -633,7 +655,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.status = status_word ? status_word : device_status_word();
-  if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
+  if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status record");
   p.N = N;
   p.BH = B * H;
   p.N_pad = N_pad;
@@ -659,7 +681,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if (!(stages & FA_BWD_DQ_CONVERT)) return FA_OK;
   const long long n8 = rows * D / 8;
   DevStatus* st_word = status_word ? status_word : device_status_word();
-  if (!st_word) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
+  if (!st_word) return set_error(FA_ERR_CUDA, "could not allocate the device status record");
   bwd::fa_bwd_dq_convert<<<(unsigned)((n8 + 255) / 256), 256, 0, stream>>>(sc.dq_acc, static_cast<__nv_bfloat16*>(dq),
                                                                            scale, n8, st_word);
   return check_cuda(cudaGetLastError(), "launch fa_bwd_dq_convert");

@@ -849,7 +849,7 @@ int prepare_fwd(fa::fwd::Params& p, bool& want_stats, const void* q, const void*
     want_stats = p.stat_rm || p.stat_rs || p.stat_branch || p.stat_ones || p.stat_min;
   }
   p.status = device_status_word();
-  if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status word");
+  if (!p.status) return set_error(FA_ERR_CUDA, "could not allocate the device status record");
   p.N = N;
   p.BH = B * H;
   p.causal = causal ? 1 : 0;

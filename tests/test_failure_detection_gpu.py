@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
 Every mbarrier wait in the kernels gives up after a time limit, raises the CTA's
-abort flag, records FA_ERR_TIMEOUT in the device status word and lets every warp
+abort flag, records FA_ERR_TIMEOUT in the device status record and lets every warp
 unwind (in-flight copies land, TMEM is freed).  A test build of the library
 (FA_TEST_HOOKS, 100 ms limit) can make the MMA warp wait on a barrier that nothing
 arrives on (forward and backward).  The call must report the timeout through
