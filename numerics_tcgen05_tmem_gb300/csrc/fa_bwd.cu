@@ -11,7 +11,8 @@
 // Three kernels on the caller's stream:
 //   fa_bwd_preprocess: delta_i = sum_c dO_ic O_ic (FP32), lse_i log2(e), both padded per
 //                      head to a multiple of 128 rows, and dQ_acc = 0
-//   fa_bwd_main:       one CTA per (b, h, 128-key tile); loops over query tiles
+//   fa_bwd_main:       work items are (b, h, 128-key tile); a CTA takes one or more items
+//                      and loops over each item's query tiles
 //   fa_bwd_dq_convert: dq = bf16(scale * dQ_acc)
 //
 // fa_bwd_main CTA organisation (512 threads, registers rebalanced per warpgroup):
@@ -24,8 +25,12 @@
 //   warps 8-11 dQ warpgroup: thread = query row; loads each dQ tile from TMEM in one
 //              round trip, hands the columns back, then reduces it into the FP32 dQ
 //              accumulator through shared-memory staging and TMA reduce-adds.
-//   warp  12   MMA issuer;  warp 13  TMA producer (Q, dO tiles and the per-tile
-//              lse / delta vectors, double-buffered);  warps 14-15 set-up/teardown only.
+//   warp  12   MMA issuer;  warp 13  TMA producer (K, V per item; Q, dO tiles and the
+//              per-tile lse / delta vectors per step);  warps 14-15 set-up/teardown only.
+// At d = 64 the grid is one CTA per SM and each CTA walks several items: the next item's K
+// and V load into a second buffer during the current item's last steps, and its first Sᵀ and
+// dPᵀ products run while the P/dS warpgroups write the current item's dK and dV.  At d = 128
+// shared memory has no room for a second K/V buffer, so each CTA takes one item.
 // Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV, and
 // at d = 64 a second S^T buffer in the last 128 columns (S^T of odd query steps).
 #include <cuda_bf16.h>
@@ -52,8 +57,9 @@ constexpr int kRegPdS = 144, kRegDQ = 152, kRegOther = 72;
 static_assert(2 * 128 * kRegPdS + 128 * kRegDQ + 128 * kRegOther <= kThreads * kRegLaunch,
               "register split exceeds the launch allocation");
 constexpr int kMaxStages = 3;   // deepest Q-tile ring (dO is single-buffered)
+constexpr int kMaxKVBufs = 2;   // most K/V buffers
 
-template <int D>
+template <int D, bool kWalk>
 struct Cfg {
   // d = 64 has room for a third Q stage and a second S^T buffer in TMEM: S_{i+2} is computed
   // into the other buffer while the P/dS warpgroups still work on step i+1
@@ -61,9 +67,15 @@ struct Cfg {
   static constexpr bool kDoubleS = (D == 64);
   static_assert(kStages <= kMaxStages, "Q ring deeper than the barrier arrays");
   static constexpr int kTileBytes = kBlock * D * 2;
+  // kWalk: a CTA walks several work items, with two K/V buffers so the next item's K and V
+  // load while it still works on the current one (K of buffer b at kKOff + b kKVBytes, V
+  // after it).  Without it a CTA takes one item and the item loops fold away.
+  static constexpr bool kMultiItem = kWalk;
+  static constexpr int kKVBufs = kWalk ? 2 : 1;
+  static_assert(kKVBufs <= kMaxKVBufs, "more K/V buffers than barriers");
+  static constexpr int kKVBytes = 2 * kTileBytes;
   static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKOff + kTileBytes;
-  static constexpr int kQOff = kVOff + kTileBytes;
+  static constexpr int kQOff = kKOff + kKVBufs * kKVBytes;
   static constexpr int kDOOff = kQOff + kStages * kTileBytes;
   static constexpr int kDSOff = kDOOff + kTileBytes;                // dS^T, 128 x 128 BF16
   // dQ staging: a ring of four 128B-swizzled slots of 32 FP32 columns x 64 rows (8 KB), the
@@ -75,6 +87,7 @@ struct Cfg {
   static constexpr int kDeltaOff = kLseOff + kStages * kBlock * 4;   // delta, per stage
   static constexpr int kBarOff = kDeltaOff + kStages * kBlock * 4;
   static constexpr int kSmemBytes = kBarOff + 256;
+  static_assert(kSmemBytes <= 227 * 1024, "backward shared-memory layout exceeds 227 KB");
   static constexpr uint32_t kTmemS = 0, kTmemDP = 128, kTmemDQ = 128, kTmemDK = 256, kTmemDV = 256 + D;
   static constexpr uint32_t kTmemS1 = kTmemDV + D;  // second S^T buffer (d = 64)
   static_assert(kTmemDV + D <= 512 && kTmemDQ + D <= kTmemDK && (!kDoubleS || kTmemS1 + 128 <= 512),
@@ -89,13 +102,16 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t kv_full;
+  uint64_t kv_full[kMaxKVBufs], kv_empty[kMaxKVBufs];
   uint64_t q_full[kMaxStages], q_empty[kMaxStages], do_full, do_empty;
-  uint64_t s_full[2], p_ready, dp_full, ds_ready, ds_empty, dq_full, dq_empty, mma_done;
+  uint64_t s_full[2], p_ready, dp_full, ds_ready, ds_empty, dq_full, dq_empty;
+  uint64_t acc_full, acc_empty;  // an item's dK, dV complete in TMEM / read out by the epilogue
+  uint64_t mma_done;
   uint64_t never;  // test builds only: a barrier nothing arrives on
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+static_assert(sizeof(Bars) <= 256, "barriers exceed their 256-byte slot in shared memory");
 
 struct Params {
   const float* lse2;    // [BH, N_pad] lse * log2(e), +inf past N
@@ -185,12 +201,25 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_convert(const float* __restrict
 }
 
 // --------------------------------------------------------------------------- main kernel
-template <int D>
+// Work item n of this CTA.  Items are the (key tile, head) pairs in key-tile order, so the
+// items with the most query tiles come first when causal; they are dealt to the CTAs in rounds
+// of gridDim.x, every other round in reverse CTA order, which evens out each CTA's total.
+// With one CTA per item (gridDim.x = items) every CTA gets exactly one.
+__device__ __forceinline__ bool work_item(const Params& p, int n, int& jt, int& bh) {
+  const long long G = gridDim.x, c = blockIdx.x;
+  const long long pos = (long long)n * G + ((n & 1) ? (G - 1 - c) : c);
+  if (pos >= (long long)p.n_tiles * p.BH) return false;
+  jt = (int)(pos / p.BH);
+  bh = (int)(pos % p.BH);
+  return true;
+}
+
+template <int D, bool kWalk>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                 const __grid_constant__ CUtensorMap tmDQ, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kWalk>;
   extern __shared__ __align__(1024) uint8_t smem[];
   // The swizzled operand layouts need a 1024-byte aligned base; there is no slack
   // for re-alignment at d = 128, so refuse to run rather than compute garbage.
@@ -201,14 +230,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars& sh = *reinterpret_cast<Bars*>(smem + C::kBarOff);
   volatile uint32_t* abort_flag = &sh.abort_flag;
   const int warp = threadIdx.x / 32;
-  const int jt = blockIdx.x / p.BH;  // key tile (ascending: heaviest first when causal)
-  const int bh = blockIdx.x % p.BH;
-  const int i0 = p.causal ? jt : 0;  // first query tile that sees this key tile
-  const int n_it = p.n_tiles - i0;
+  // Per-step barriers alternate phases over the CTA's query steps counted across its items
+  // (g below); per-item barriers over its items (n).
 
   if (threadIdx.x == 0) {
     sh.abort_flag = 0;
-    mbar_init(&sh.kv_full, 1);
+    for (int b = 0; b < C::kKVBufs; ++b) {
+      mbar_init(&sh.kv_full[b], 1);
+      mbar_init(&sh.kv_empty[b], 1);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&sh.q_full[s], 1);
       mbar_init(&sh.q_empty[s], 1);
@@ -223,6 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.ds_empty, 1);
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.dq_empty, kBlock);
+    mbar_init(&sh.acc_full, 1);
+    mbar_init(&sh.acc_empty, 2 * kBlock);
     mbar_init(&sh.mma_done, 1);
     mbar_init(&sh.never, 1);
     fence_barrier_init();
@@ -247,97 +279,126 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::kTileBytes);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(smem + C::kKOff + c * 16384, &tmK, &sh.kv_full, c * 64, jt * kBlock, bh);
-        tma_load_3d(smem + C::kVOff + c * 16384, &tmV, &sh.kv_full, c * 64, jt * kBlock, bh);
-      }
-      const size_t stat_base = (size_t)bh * p.N_pad;
-      int nq = 0, ndo = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        const int row0 = (i0 + it) * kBlock;
-        if (!mbar_wait(&sh.q_empty[s], ph ^ 1, abort_flag, p.status)) break;
-        if (!FA_BOUNDS_OK(row0 < p.N_pad && (long long)stat_base + row0 + kBlock <= (long long)p.BH * p.N_pad,
-                          p.status, kSiteBwdQRow, row0))
-          break;
-        // Q tile plus the tile's 128 padded lse*log2(e) and delta values (512 B each)
-        mbar_arrive_expect_tx(&sh.q_full[s], C::kTileBytes + 2 * kBlock * 4);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::kQOff + s * C::kTileBytes + c * 16384, &tmQ, &sh.q_full[s], c * 64, row0, bh);
-        bulk_load(smem + C::kLseOff + s * kBlock * 4, p.lse2 + stat_base + row0, kBlock * 4, &sh.q_full[s]);
-        bulk_load(smem + C::kDeltaOff + s * kBlock * 4, p.delta + stat_base + row0, kBlock * 4, &sh.q_full[s]);
-        nq = it + 1;
-        if (!mbar_wait(&sh.do_empty, (it & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + C::kDOOff + c * 16384, &tmDO, &sh.do_full, c * 64, row0, bh);
-        ndo = it + 1;
+      int g = 0;                     // query steps so far, over all items
+      int nq = 0, ndo = 0, nkv = 0;  // loads issued: Q tiles, dO tiles, K/V pairs
+      bool ok = true;
+      for (int n = 0; ok && (C::kMultiItem || n == 0); ++n) {
+        int jt, bh;
+        if (!work_item(p, n, jt, bh)) break;
+        const int b = n % C::kKVBufs;
+        // the buffer's previous item has issued its last MMA reading K or V
+        if (!(ok = mbar_wait(&sh.kv_empty[b], ((n / C::kKVBufs) & 1) ^ 1, abort_flag, p.status))) break;
+        mbar_arrive_expect_tx(&sh.kv_full[b], 2 * C::kTileBytes);
+        uint8_t* kv = smem + C::kKOff + b * C::kKVBytes;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(kv + c * 16384, &tmK, &sh.kv_full[b], c * 64, jt * kBlock, bh);
+          tma_load_3d(kv + C::kTileBytes + c * 16384, &tmV, &sh.kv_full[b], c * 64, jt * kBlock, bh);
+        }
+        nkv = n + 1;
+        const int i0 = p.causal ? jt : 0;  // first query tile that sees this key tile
+        const int n_it = p.n_tiles - i0;
+        const size_t stat_base = (size_t)bh * p.N_pad;
+        for (int it = 0; it < n_it; ++it, ++g) {
+          const int s = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
+          const int row0 = (i0 + it) * kBlock;
+          if (!(ok = mbar_wait(&sh.q_empty[s], ph ^ 1, abort_flag, p.status))) break;
+          if (!FA_BOUNDS_OK(row0 < p.N_pad && (long long)stat_base + row0 + kBlock <= (long long)p.BH * p.N_pad,
+                            p.status, kSiteBwdQRow, row0)) {
+            ok = false;
+            break;
+          }
+          // Q tile plus the tile's 128 padded lse*log2(e) and delta values (512 B each)
+          mbar_arrive_expect_tx(&sh.q_full[s], C::kTileBytes + 2 * kBlock * 4);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::kQOff + s * C::kTileBytes + c * 16384, &tmQ, &sh.q_full[s], c * 64, row0, bh);
+          bulk_load(smem + C::kLseOff + s * kBlock * 4, p.lse2 + stat_base + row0, kBlock * 4, &sh.q_full[s]);
+          bulk_load(smem + C::kDeltaOff + s * kBlock * 4, p.delta + stat_base + row0, kBlock * 4, &sh.q_full[s]);
+          nq = g + 1;
+          if (!(ok = mbar_wait(&sh.do_empty, (g & 1) ^ 1, abort_flag, p.status))) break;
+          mbar_arrive_expect_tx(&sh.do_full, C::kTileBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + C::kDOOff + c * 16384, &tmDO, &sh.do_full, c * 64, row0, bh);
+          ndo = g + 1;
+        }
       }
       if (*abort_flag) {
         // let copies still in flight land before the CTA's shared memory goes away
         volatile uint32_t ignore_abort = 0;
-        mbar_wait(&sh.kv_full, 0, &ignore_abort, p.status);
-        for (int it = max(0, nq - C::kStages); it < nq; ++it)
-          mbar_wait(&sh.q_full[it % C::kStages], (it / C::kStages) & 1, &ignore_abort, p.status);
+        for (int n = max(0, nkv - C::kKVBufs); n < nkv; ++n)
+          mbar_wait(&sh.kv_full[n % C::kKVBufs], (n / C::kKVBufs) & 1, &ignore_abort, p.status);
+        for (int i = max(0, nq - C::kStages); i < nq; ++i)
+          mbar_wait(&sh.q_full[i % C::kStages], (i / C::kStages) & 1, &ignore_abort, p.status);
         if (ndo > 0) mbar_wait(&sh.do_full, (ndo - 1) & 1, &ignore_abort, p.status);
       }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      const uint32_t sK = smem_u32(smem + C::kKOff), sV = smem_u32(smem + C::kVOff);
       const uint32_t sQ = smem_u32(smem + C::kQOff), sDO = smem_u32(smem + C::kDOOff);
       const uint32_t sDS = smem_u32(smem + C::kDSOff);
       // K-major operand with D (or 128) columns: 16 KB per 64 columns, 32 B per k-step
       auto kmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024); };
       // MN-major operand with 128 K rows: 2 KB per k-step, 16 KB between 64-column blocks
       auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, 16384, 1024); };
-      bool ok = mbar_wait(&sh.kv_full, 0, abort_flag, p.status);
+      bool ok = true;
 #ifdef FA_TEST_HOOKS
       // failure-detection test: wait on a barrier nothing arrives on; the bounded wait runs
       // out, raises the CTA's abort flag and records a timeout, and every warp unwinds
-      if (p.inject_stall) ok = ok && mbar_wait(&sh.never, 0, abort_flag, p.status);
+      if (p.inject_stall) ok = mbar_wait(&sh.never, 0, abort_flag, p.status);
 #endif
-      auto issue_s = [&](int it) {  // S^T = K_j Q_i^T
-        const int s = it % C::kStages;
-        if (!(ok = mbar_wait(&sh.q_full[s], (it / C::kStages) & 1, abort_flag, p.status))) return;
-        tc_fence_after();
-        const uint32_t q = sQ + s * C::kTileBytes;
+      int g0 = 0;  // query steps before the current item, over all items
+      for (int n = 0; ok && (C::kMultiItem || n == 0); ++n) {
+        int jt, bh;
+        if (!work_item(p, n, jt, bh)) break;
+        const int b = n % C::kKVBufs;
+        const uint32_t sK = smem_u32(smem + C::kKOff + b * C::kKVBytes), sV = sK + C::kTileBytes;
+        const int n_it = p.n_tiles - (p.causal ? jt : 0);
+        if (!(ok = mbar_wait(&sh.kv_full[b], (n / C::kKVBufs) & 1, abort_flag, p.status))) break;
+        // the lambdas take the item's step `it`; barriers and buffers go by the CTA's step g0 + it
+        auto issue_s = [&](int it) {  // S^T = K_j Q_i^T
+          const int g = g0 + it;
+          const int s = g % C::kStages;
+          if (!(ok = mbar_wait(&sh.q_full[s], (g / C::kStages) & 1, abort_flag, p.status))) return;
+          tc_fence_after();
+          const uint32_t q = sQ + s * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::s_col(it), kmaj(sK, kk), kmaj(q, kk), C::kIdescSq, kk > 0);
-        tc_commit(&sh.s_full[C::s_slot(it)]);
-      };
-      const uint32_t dO = sDO;
-      // dP^T = V_j dO_i^T into dP^T's columns (which held dQ_{i-1}: wait until drained)
-      auto issue_dp = [&](int it) {
-        if (!(ok = mbar_wait(&sh.do_full, it & 1, abort_flag, p.status))) return;
-        if (it > 0 && !(ok = mbar_wait(&sh.dq_empty, (it - 1) & 1, abort_flag, p.status))) return;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::s_col(g), kmaj(sK, kk), kmaj(q, kk), C::kIdescSq, kk > 0);
+          tc_commit(&sh.s_full[C::s_slot(g)]);
+        };
+        // dP^T = V_j dO_i^T into dP^T's columns (which held dQ of the step before: wait until drained)
+        auto issue_dp = [&](int it) {
+          const int g = g0 + it;
+          if (!(ok = mbar_wait(&sh.do_full, g & 1, abort_flag, p.status))) return;
+          if (g > 0 && !(ok = mbar_wait(&sh.dq_empty, (g - 1) & 1, abort_flag, p.status))) return;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) mma_ss(tmem + C::kTmemDP, kmaj(sV, kk), kmaj(dO, kk), C::kIdescSq, kk > 0);
-        tc_commit(&sh.dp_full);
-      };
-      // dV += P^T dO_i: P^T (BF16) sits in S^T's columns 0-31 (queries 0-63) and
-      // 64-95 (queries 64-127); 8 columns per k-step of 16 queries
-      auto issue_dv = [&](int it) {
-        if (!(ok = mbar_wait(&sh.do_full, it & 1, abort_flag, p.status))) return;
-        if (!(ok = mbar_wait(&sh.p_ready, it & 1, abort_flag, p.status))) return;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::kTmemDP, kmaj(sV, kk), kmaj(sDO, kk), C::kIdescSq, kk > 0);
+          tc_commit(&sh.dp_full);
+        };
+        // dV += P^T dO_i: P^T (BF16) sits in S^T's columns 0-31 (queries 0-63) and
+        // 64-95 (queries 64-127); 8 columns per k-step of 16 queries.  An item's first dV
+        // product overwrites the accumulator: the previous item's dK and dV must be read out.
+        auto issue_dv = [&](int it) {
+          const int g = g0 + it;
+          if (!(ok = mbar_wait(&sh.do_full, g & 1, abort_flag, p.status))) return;
+          if (!(ok = mbar_wait(&sh.p_ready, g & 1, abort_flag, p.status))) return;
+          if (it == 0 && n > 0 && !(ok = mbar_wait(&sh.acc_empty, (n - 1) & 1, abort_flag, p.status))) return;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk)
-          mma_ts(tmem + C::kTmemDV, tmem + C::s_col(it) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(dO, kk),
-                 C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
-      };
-      // Issue order (same-thread MMAs execute in order):
-      //   S_0 dP_0 dV_0 S_1 | dK_0 dQ_0 dP_1 dV_1 S_2 | dK_1 dQ_1 dP_2 dV_2 S_3 | ...
-      // dP_{i+1} needs only dO and the drained dQ_i columns, so it runs while the softmax
-      // warpgroups compute P_{i+1}; dV_{i+1} follows once P_{i+1} is in TMEM.  With two S^T
-      // buffers (d = 64) S_{i+2} goes before dV_{i+1}: its buffer's last reader, dV_i, was
-      // issued a round earlier.
-      if (ok && n_it > 0) {
+          for (int kk = 0; kk < kBlock / 16; ++kk)
+            mma_ts(tmem + C::kTmemDV, tmem + C::s_col(g) + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(sDO, kk),
+                   C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
+        };
+        // Issue order (same-thread MMAs execute in order):
+        //   S_0 dP_0 dV_0 S_1 | dK_0 dQ_0 dP_1 dV_1 S_2 | dK_1 dQ_1 dP_2 dV_2 S_3 | ...
+        // dP_{i+1} needs only dO and the drained dQ_i columns, so it runs while the softmax
+        // warpgroups compute P_{i+1}; dV_{i+1} follows once P_{i+1} is in TMEM.  With two S^T
+        // buffers (d = 64) S_{i+2} goes before dV_{i+1}: its buffer's last reader, dV_i, was
+        // issued a round earlier.  The next item's S_0, dP_0 (and S_1) need none of this item's
+        // accumulators, so they run while its dK and dV are written out.
         tc_fence_after();
         issue_s(0);
         if (ok) issue_dp(0);
@@ -345,41 +406,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) issue_dv(0);
         if (ok) tc_commit(&sh.do_empty);
         if (!C::kDoubleS && ok && n_it > 1) issue_s(1);
-      }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t q = sQ + s * C::kTileBytes;
-        // dK += dS^T Q_i ;  dQ_i = dS K_j
-        if (!(ok = mbar_wait(&sh.ds_ready, it & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        // dS^T (BF16) sits in dP^T's columns 0-31 (queries 0-63) and 64-95 (queries 64-127);
-        // reading it from TMEM spares shared-memory bandwidth (dQ, issued next, overwrites
-        // those columns only after this MMA has read them: same-thread MMAs run in order)
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int g = g0 + it;
+          const int s = g % C::kStages;
+          const uint32_t q = sQ + s * C::kTileBytes;
+          // dK += dS^T Q_i ;  dQ_i = dS K_j
+          if (!(ok = mbar_wait(&sh.ds_ready, g & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          // dS^T (BF16) sits in dP^T's columns 0-31 (queries 0-63) and 64-95 (queries 64-127);
+          // reading it from TMEM spares shared-memory bandwidth (dQ, issued next, overwrites
+          // those columns only after this MMA has read them: same-thread MMAs run in order)
 #pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk)
-          mma_ts(tmem + C::kTmemDK, tmem + C::kTmemDP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(q, kk),
-                 C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBlock / 16; ++kk)
+            mma_ts(tmem + C::kTmemDK, tmem + C::kTmemDP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), mnmaj(q, kk),
+                   C::kIdescKV, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk)
-          mma_ss(tmem + C::kTmemDQ, mnmaj(sDS, kk), mnmaj(sK, kk), C::kIdescQ, kk > 0);
-        tc_commit(&sh.q_empty[s]);
-        tc_commit(&sh.ds_empty);
-        tc_commit(&sh.dq_full);
-        if (it + 1 < n_it) {
-          issue_dp(it + 1);
-          if (!ok) break;
-          if (C::kDoubleS && it + 2 < n_it) {
-            issue_s(it + 2);
+          for (int kk = 0; kk < kBlock / 16; ++kk)
+            mma_ss(tmem + C::kTmemDQ, mnmaj(sDS, kk), mnmaj(sK, kk), C::kIdescQ, kk > 0);
+          tc_commit(&sh.q_empty[s]);
+          tc_commit(&sh.ds_empty);
+          tc_commit(&sh.dq_full);
+          if (it + 1 < n_it) {
+            issue_dp(it + 1);
             if (!ok) break;
-          }
-          issue_dv(it + 1);
-          if (!ok) break;
-          tc_commit(&sh.do_empty);
-          if (!C::kDoubleS && it + 2 < n_it) {
-            issue_s(it + 2);
+            if (C::kDoubleS && it + 2 < n_it) {
+              issue_s(it + 2);
+              if (!ok) break;
+            }
+            issue_dv(it + 1);
             if (!ok) break;
+            tc_commit(&sh.do_empty);
+            if (!C::kDoubleS && it + 2 < n_it) {
+              issue_s(it + 2);
+              if (!ok) break;
+            }
           }
         }
+        if (!ok) break;
+        // the item's dK and dV are complete once its last products finish; so are its K and V reads
+        tc_commit(&sh.acc_full);
+        tc_commit(&sh.kv_empty[b]);
+        g0 += n_it;
       }
       tc_commit(&sh.mma_done);
       {
@@ -403,14 +470,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* ds_row = smem + C::kDSOff + h * 16384 + r * 128;
     const uint32_t sw = (uint32_t)(r & 7);
     bool ok = true;
+    int g0 = 0;  // query steps before the current item, over all items
+    for (int n = 0; ok && (C::kMultiItem || n == 0); ++n) {
+    int jt, bh;
+    if (!work_item(p, n, jt, bh)) break;
+    const int n_it = p.n_tiles - (p.causal ? jt : 0);
     for (int it = 0; it < n_it; ++it) {
-      const int s = it % C::kStages;
+      const int g = g0 + it;
+      const int s = g % C::kStages;
       const bool diag = p.causal && it == 0;  // query tile i0 == key tile jt: mask q < key
-      const uint32_t tS = tS0 + C::s_col(it);
+      const uint32_t tS = tS0 + C::s_col(g);
       const float4* lse4 = reinterpret_cast<const float4*>(smem + C::kLseOff + s * kBlock * 4) + 16 * h;
       const float4* dl4 = reinterpret_cast<const float4*>(smem + C::kDeltaOff + s * kBlock * 4) + 16 * h;
-      if (!(ok = mbar_wait(&sh.q_full[s], (it / C::kStages) & 1, abort_flag, p.status))) break;
-      if (!(ok = mbar_wait(&sh.s_full[C::s_slot(it)], C::s_parity(it), abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.q_full[s], (g / C::kStages) & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.s_full[C::s_slot(g)], C::s_parity(g), abort_flag, p.status))) break;
       tc_fence_after();
       // P^T = exp2(S^T c - lse_q log2 e); padded queries carry lse = +inf -> 0
       // this warpgroup's 64 columns of the row in one round trip
@@ -448,8 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.p_ready);
       // dS^T = P^T o (dP^T - delta_q), written 32 queries at a time into the swizzled
       // dS^T tile once the previous step's dK / dQ MMAs have finished reading it
-      if (!(ok = mbar_wait(&sh.dp_full, it & 1, abort_flag, p.status))) break;
-      if (it > 0 && !(ok = mbar_wait(&sh.ds_empty, (it - 1) & 1, abort_flag, p.status))) break;
+      if (!(ok = mbar_wait(&sh.dp_full, g & 1, abort_flag, p.status))) break;
+      if (g > 0 && !(ok = mbar_wait(&sh.ds_empty, (g - 1) & 1, abort_flag, p.status))) break;
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -495,9 +568,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&sh.ds_ready);
     }
+    if (!ok) break;
     // ------------------------------------------------------------------ dK (h = 0) / dV (h = 1) epilogue
-    if (ok && n_it > 0 && mbar_wait(&sh.mma_done, 0, abort_flag, p.status)) {
-      tc_fence_after();
+    if (!(ok = mbar_wait(&sh.acc_full, n & 1, abort_flag, p.status))) break;
+    tc_fence_after();
+    {
       const int key = jt * kBlock + r;
       const bool valid = key < p.N;
       const size_t orow = ((size_t)bh * p.N + (valid ? key : 0)) * D;
@@ -525,7 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i) dst[i] = pkd[i];
         }
       }
+      // this row of dK / dV has been read: the next item's first dV product may overwrite it
+      tc_fence_before();
+      mbar_arrive(&sh.acc_empty);
       report_nonfinite(valid ? bad : 0u, p.status, h == 0 ? kOutDk : kOutDv);
+    }
+    g0 += n_it;
     }
   } else {
     // ------------------------------------------------------------------ dQ warpgroup
@@ -544,8 +624,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tDQ = tmem + C::kTmemDQ + ((uint32_t)lane_base << 16);
     const uint32_t sw = (uint32_t)(r & 7);
     int g_total = 0;  // 32-column groups pushed so far (slot pair = g_total % 2)
+    int g0 = 0;       // query steps before the current item, over all items
+    bool ok = true;
+    for (int n = 0; ok && (C::kMultiItem || n == 0); ++n) {
+    int jt, bh;
+    if (!work_item(p, n, jt, bh)) break;
+    const int i0 = p.causal ? jt : 0;
+    const int n_it = p.n_tiles - i0;
     for (int it = 0; it < n_it; ++it) {
-      if (!mbar_wait(&sh.dq_full, it & 1, abort_flag, p.status)) break;
+      if (!(ok = mbar_wait(&sh.dq_full, (g0 + it) & 1, abort_flag, p.status))) break;
       tc_fence_after();
       const int q0 = (i0 + it) * kBlock;
       uint32_t w[D];
@@ -577,6 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_commit_group();
         }
       }
+    }
+    g0 += n_it;
     }
     // the accumulator must hold every reduction before the CTA retires
     if (leader) bulk_wait_all();
@@ -623,12 +712,39 @@ Scratch carve_scratch(void* base, int B, int H, int N, int d) {
   return s;
 }
 
+template <int D, bool kWalk>
+int launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                const CUtensorMap& tdq, const fa::bwd::Params& p, cudaStream_t stream) {
+  using namespace fa;
+  using C = bwd::Cfg<D, kWalk>;
+  auto kern = bwd::fa_bwd_main<D, kWalk>;
+  // setmaxnreg.inc waits until the block's launch registers cover the new split: refuse to
+  // launch a build whose launch allocation is smaller than the split needs
+  constexpr int kSplit = 2 * 128 * bwd::kRegPdS + 128 * bwd::kRegDQ + 128 * bwd::kRegOther;
+  static std::atomic<uint64_t> prepared{0};
+  int rc = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, bwd::kThreads, kSplit,
+                          "backward kernel", &prepared);
+  if (rc) return rc;
+  const long long items = (long long)p.n_tiles * p.BH;
+  long long grid = items;
+  if (kWalk) {
+    const int sms = sm_count();
+    if (sms > 0 && sms < grid) grid = sms;
+#ifdef FA_TEST_HOOKS
+    // item-walk test: any grid from 1 CTA (every item in one CTA) up to one CTA per item
+    const char* grid_env = getenv("FA_TEST_BWD_GRID");
+    if (grid_env && atoll(grid_env) > 0) grid = atoll(grid_env) < items ? atoll(grid_env) : items;
+#endif
+  }
+  kern<<<(unsigned)grid, bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
+  return check_cuda(cudaGetLastError(), "launch fa_bwd_main");
+}
+
 template <int D>
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO, void* dq,
                void* dk, void* dv, float* delta_out, int B, int H, int N, int causal, float scale,
                const Scratch& sc, cudaStream_t stream, int stages, fa::DevStatus* status_word = nullptr) {
   using namespace fa;
-  using C = bwd::Cfg<D>;
   const long long rows = (long long)B * H * N;
   int rc;
   const int N_pad = (N + bwd::kBlock - 1) / bwd::kBlock * bwd::kBlock;
@@ -667,16 +783,19 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   const char* inject = getenv("FA_TEST_INJECT_STALL");
   p.inject_stall = (inject && inject[0] == '1') ? 1 : 0;
 #endif
-  auto kern = bwd::fa_bwd_main<D>;
-  // setmaxnreg.inc waits until the block's launch registers cover the new split: refuse to
-  // launch a build whose launch allocation is smaller than the split needs
-  constexpr int kSplit = 2 * 128 * bwd::kRegPdS + 128 * bwd::kRegDQ + 128 * bwd::kRegOther;
-  static std::atomic<uint64_t> prepared{0};
-  if ((rc = prepare_kernel(reinterpret_cast<const void*>(kern), C::kSmemBytes, bwd::kThreads, kSplit,
-                           "backward kernel", &prepared)))
-    return rc;
-  kern<<<(unsigned)(p.n_tiles * p.BH), bwd::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdq, p);
-  if ((rc = check_cuda(cudaGetLastError(), "launch fa_bwd_main"))) return rc;
+  // d = 64 with up to kItemWalkMaxTiles key tiles: one CTA per SM walking several items (the
+  // next item's K/V load overlaps the current one; measured +7-8 % at 1024 and 2048 tokens,
+  // +3 % at 4096).  Longer rows have few, long items; one CTA per item (placed by the
+  // hardware as SMs free up) is 1-3 % faster there.  d = 128 has no room for a second K/V
+  // buffer: one CTA per item.
+  constexpr int kItemWalkMaxTiles = 32;
+  if constexpr (D == 64) {
+    if (p.n_tiles <= kItemWalkMaxTiles) rc = launch_main<D, true>(tq, tk, tv, tdo, tdq, p, stream);
+    else rc = launch_main<D, false>(tq, tk, tv, tdo, tdq, p, stream);
+  } else {
+    rc = launch_main<D, false>(tq, tk, tv, tdo, tdq, p, stream);
+  }
+  if (rc) return rc;
   }
   if (!(stages & FA_BWD_DQ_CONVERT)) return FA_OK;
   const long long n8 = rows * D / 8;
