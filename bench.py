@@ -337,7 +337,9 @@ def run_native(args):
 
     e2e_run(3)
     barrier()
-    e2e_ms = max_over_ranks(e2e_run(E) / E, dist, dev)
+    # the faster of two runs: the host side (pinned memory, the link) is shared with the rest
+    # of the machine, and one transient has been seen to triple a single run's time
+    e2e_ms = max_over_ranks(min(e2e_run(E), e2e_run(E)) / E, dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = sum(t.numel() * t.element_size() for t in host_out[0])
 
