@@ -27,10 +27,11 @@
 //              accumulator through shared-memory staging and TMA reduce-adds.
 //   warp  12   MMA issuer;  warp 13  TMA producer (K, V per item; Q, dO tiles and the
 //              per-tile lse / delta vectors per step);  warps 14-15 set-up/teardown only.
-// At d = 64 the grid is one CTA per SM and each CTA walks several items: the next item's K
-// and V load into a second buffer during the current item's last steps, and its first Sᵀ and
-// dPᵀ products run while the P/dS warpgroups write the current item's dK and dV.  At d = 128
-// shared memory has no room for a second K/V buffer, so each CTA takes one item.
+// At d = 64 with up to 4096 keys the grid is one CTA per SM and each CTA walks several items
+// (fa_bwd_main<64, true>): the next item's K and V load into a second buffer during the
+// current item's last steps, and its first S^T and dP^T products run while the P/dS
+// warpgroups write the current item's dK and dV.  Longer rows, and d = 128 (whose shared
+// memory has no room for a second K/V buffer), take one CTA per item.
 // Tensor memory (512 columns): S^T | dP^T (the dQ tile reuses these columns) | dK | dV, and
 // at d = 64 a second S^T buffer in the last 128 columns (S^T of odd query steps).
 #include <cuda_bf16.h>
