@@ -91,3 +91,24 @@ def test_fp8_forward_trips_no_index_check(dbg, N, d):
     o_ref, lse_ref = binding.forward_fp8(q8, k8, v8, desc, causal=True, scale=w.scale, stable=1, beta=1.25)
     binding.device_status()
     assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_item_walk_trips_no_index_check(dbg, causal):
+    # d = 64 with more (key tile, head) items than SMs: every CTA of the debug build walks
+    # several items, so the index checks also cover the walk's later items
+    w = inputs.random_case(4, 40, 700, 64, causal, seed=707 + causal, std=1.1)
+    q, k, v, do = to_dev(w)
+    B, H, N, d = q.shape
+    assert B * H * ((N + 127) // 128) > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    o, lse = binding.forward(q, k, v, causal=causal, scale=w.scale, stable=1, beta=1.25)
+    ws = torch.empty(dbg.fa_bwd_workspace_size(B, H, N, d), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    assert dbg.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), do.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), None, B, H, N, d, int(causal), w.scale,
+                      ws.data_ptr(), ws.numel(), _stream()) == binding.FA_OK
+    _assert_clean(dbg)
+    dq_ref, dk_ref, dv_ref = binding.backward(q, k, v, o, lse, do, causal=causal, scale=w.scale)
+    binding.device_status()
+    assert torch.equal(dk, dk_ref) and torch.equal(dv, dv_ref)
+    assert rel_fro(dq, dq_ref) <= 1e-3
