@@ -95,6 +95,19 @@ def test_extreme_16k_sampled_head(causal, stable):
     check(ws, res, oracle_grads(ws), sel=lambda t: t[:, [9]])
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("N", [4096, 4097])
+def test_d64_item_walk_length_boundary_sampled_head(N, causal):
+    # d = 64: up to 4096 keys the backward runs one CTA per SM walking the (key tile, head)
+    # items (here 512 or more of them), from 4097 keys one CTA per item; both against the oracle
+    w = inputs.random_case(2, 8, N, 64, causal, seed=N + 31 * causal, std=1.0)
+    res = run_fwd_bwd(w)
+    b, h = 1, 5
+    sub = inputs.Workload("sub", w.q[b:b + 1, h:h + 1], w.k[b:b + 1, h:h + 1], w.v[b:b + 1, h:h + 1],
+                          w.do[b:b + 1, h:h + 1], causal, w.scale, 1, 1.25)
+    check(sub, res, oracle_grads(sub), sel=lambda t: t[b:b + 1, h:h + 1])
+
+
 def test_repeat_calls_reuse_workspace():
     w = inputs.gpt2_small(B=1, H=4, N=1024)
     q, k, v, do = to_dev(w)
