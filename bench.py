@@ -401,7 +401,8 @@ def run_native(args):
     configs = None
     if not args.no_configs:
         keep = ("workload", "what", "fwd_stable0_tflops", "fwd_stable0_frac", "fwd_stable1_tflops",
-                "fwd_stable1_frac", "bwd_tflops", "bwd_frac", "fp8_fwd_stable1_tflops", "l2_flush")
+                "fwd_stable1_frac", "bwd_tflops", "bwd_frac", "fp8_fwd_stable0_tflops", "fp8_fwd_stable1_tflops",
+                "l2_flush")
         configs = [{k2: r[k2] for k2 in keep if k2 in r} for r in measure_configs()]
 
     peaks = load_peaks()
@@ -564,10 +565,11 @@ def measure_configs(with_fp8=True, R=10):
         if with_fp8:
             (q8, dq8), (k8, dk8), (v8, dv8) = (binding.quantize_fp8(t) for t in (q, k, v))
             desc = torch.cat([dq8, dk8, dv8])
-            ms8 = timed(lambda: binding.forward_fp8(q8, k8, v8, desc, causal=w.causal, scale=w.scale, stable=1,
-                                                    beta=w.beta))
-            line["fp8_fwd_stable1_ms"] = round(ms8, 4)
-            line["fp8_fwd_stable1_tflops"] = round(ff / (ms8 * 1e-3) / 1e12, 1)
+            for stable in (0, 1):
+                ms8 = timed(lambda: binding.forward_fp8(q8, k8, v8, desc, causal=w.causal, scale=w.scale,
+                                                        stable=stable, beta=w.beta))
+                line[f"fp8_fwd_stable{stable}_ms"] = round(ms8, 4)
+                line[f"fp8_fwd_stable{stable}_tflops"] = round(ff / (ms8 * 1e-3) / 1e12, 1)
             del q8, k8, v8
         binding.device_status()
         rows.append(line)
