@@ -524,27 +524,27 @@ __global__ void __launch_bounds__(Shape<kT>::kThreads, Shape<kT>::kCtasPerSm)
           // one of those rows needs (exact -- a skipped chunk has no entry equal to bm in
           // any row that uses bc).
           const bool need = bm >= rm;
-          uint32_t neg0 = 0, neg1 = 0;
+          float c0s = 0.f, c1s = 0.f, c2s = 0.f, c3s = 0.f;  // two independent pair sums
 #pragma unroll
           for (int c0 = 0; c0 < kBlockN / 32; ++c0) {
             if (__any_sync(0xffffffffu, need && pmax[c0] == bm)) {
 #pragma unroll
               for (int i = c0 * 32; i < c0 * 32 + 32; i += 4) {
-                neg0 += eq_mask(sv[i], bm) + eq_mask(sv[i + 1], bm);
-                neg1 += eq_mask(sv[i + 2], bm) + eq_mask(sv[i + 3], bm);
+                add2(c0s, c1s, c0s, c1s, eq_one(sv[i], bm), eq_one(sv[i + 1], bm));
+                add2(c2s, c3s, c2s, c3s, eq_one(sv[i + 2], bm), eq_one(sv[i + 3], bm));
               }
             }
           }
-          bc = (bm == -INFINITY) ? 0 : -(int)(neg0 + neg1);
+          bc = (bm == -INFINITY) ? 0 : (int)((c0s + c1s) + (c2s + c3s));
         } else if (kStable == 2 || __any_sync(0xffffffffu, bm >= rm)) {
-          // each equality gives an all-ones mask (-1); two masks per three-input add
-          uint32_t neg0 = 0, neg1 = 0;
+          // each equality gives 1.0, summed in FP32 pairs (exact)
+          float c0s = 0.f, c1s = 0.f, c2s = 0.f, c3s = 0.f;
 #pragma unroll
           for (int i = 0; i < kBlockN; i += 4) {
-            neg0 += eq_mask(sv[i], bm) + eq_mask(sv[i + 1], bm);
-            neg1 += eq_mask(sv[i + 2], bm) + eq_mask(sv[i + 3], bm);
+            add2(c0s, c1s, c0s, c1s, eq_one(sv[i], bm), eq_one(sv[i + 1], bm));
+            add2(c2s, c3s, c2s, c3s, eq_one(sv[i + 2], bm), eq_one(sv[i + 3], bm));
           }
-          bc = (bm == -INFINITY) ? 0 : -(int)(neg0 + neg1);
+          bc = (bm == -INFINITY) ? 0 : (int)((c0s + c1s) + (c2s + c3s));
         }
         const float rm_new = fmaxf(rm, bm);
         rs = ((rm == rm_new) ? rs : 0) + ((bm == rm_new) ? bc : 0);
