@@ -483,25 +483,24 @@ __global__ void __launch_bounds__(Shape<kT>::kThreads, Shape<kT>::kCtasPerSm)
 #pragma unroll
         for (int i = 0; i < kBlockN; ++i) sv[i] = (i < lim) ? sv[i] : -INFINITY;
       }
-      // block max: from the loads' reductions when no row of the warp has a masked column,
-      // else over the masked values with 3-input max in four independent chains
-      float bm;
+      // block max and each 32-column chunk's maximum: from the loads' reductions when no row
+      // of the warp has a masked column, else over the masked values (3-input max, one
+      // independent chain per chunk)
+      float pm[kBlockN / 32];
       const bool unmasked = __all_sync(0xffffffffu, lim >= kBlockN);
       if (unmasked) {
-        bm = fmaxf(max3f(pmax[0], pmax[1], pmax[2]), pmax[3]);
-      } else {
-        float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-        for (int i = 4; i < kBlockN - 4; i += 8) {
-          mx0 = max3f(mx0, sv[i], sv[i + 1]);
-          mx1 = max3f(mx1, sv[i + 2], sv[i + 3]);
-          mx2 = max3f(mx2, sv[i + 4], sv[i + 5]);
-          mx3 = max3f(mx3, sv[i + 6], sv[i + 7]);
+        for (int c0 = 0; c0 < kBlockN / 32; ++c0) pm[c0] = pmax[c0];
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < kBlockN / 32; ++c0) {
+          float mx = max3f(sv[32 * c0], sv[32 * c0 + 1], sv[32 * c0 + 2]);
+#pragma unroll
+          for (int i = 32 * c0 + 3; i < 32 * c0 + 31; i += 2) mx = max3f(mx, sv[i], sv[i + 1]);
+          pm[c0] = fmaxf(mx, sv[32 * c0 + 31]);
         }
-        mx0 = max3f(mx0, sv[kBlockN - 4], sv[kBlockN - 3]);
-        mx1 = max3f(mx1, sv[kBlockN - 2], sv[kBlockN - 1]);
-        bm = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
       }
+      const float bm = fmaxf(max3f(pm[0], pm[1], pm[2]), pm[3]);
       if constexpr (kStats) {
         // masked entries hold -inf; they never count as the row's minimum
         float mn0 = INFINITY, mn1 = INFINITY;
@@ -516,36 +515,24 @@ __global__ void __launch_bounds__(Shape<kT>::kThreads, Shape<kT>::kCtasPerSm)
       int bc = 0;
       if constexpr (kStable != 0 || kStats) {
         // running (max, count) merge: rs' = [rm == rm'] rs + [bm == rm'] bc.  The block's
-        // count only matters when bm reaches the running max (or, block-locally, always),
-        // so a warp whose rows all have bm < rm skips counting.
-        if (kStable != 2 && unmasked) {
-          // Only a 32-column chunk whose load-time maximum equals the block maximum can hold
-          // it, and only rows with bm >= rm need the count: the warp counts just the chunks
-          // one of those rows needs (exact -- a skipped chunk has no entry equal to bm in
-          // any row that uses bc).
-          const bool need = bm >= rm;
-          float c0s = 0.f, c1s = 0.f, c2s = 0.f, c3s = 0.f;  // two independent pair sums
+        // count only matters when bm reaches the running max (or, block-locally, always).
+        // Only a chunk whose maximum equals the block maximum can hold it, so the warp counts
+        // just the chunks one of the rows that need the count needs (exact -- a skipped chunk
+        // has no entry equal to bm in any row that uses bc); a warp whose rows all have
+        // bm < rm counts nothing.  Each equality gives 1.0, summed in FP32 pairs (exact).
+        const bool need = (kStable == 2) || (bm >= rm);
+        float c0s = 0.f, c1s = 0.f, c2s = 0.f, c3s = 0.f;  // two independent pair sums
 #pragma unroll
-          for (int c0 = 0; c0 < kBlockN / 32; ++c0) {
-            if (__any_sync(0xffffffffu, need && pmax[c0] == bm)) {
+        for (int c0 = 0; c0 < kBlockN / 32; ++c0) {
+          if (__any_sync(0xffffffffu, need && pm[c0] == bm)) {
 #pragma unroll
-              for (int i = c0 * 32; i < c0 * 32 + 32; i += 4) {
-                add2(c0s, c1s, c0s, c1s, eq_one(sv[i], bm), eq_one(sv[i + 1], bm));
-                add2(c2s, c3s, c2s, c3s, eq_one(sv[i + 2], bm), eq_one(sv[i + 3], bm));
-              }
+            for (int i = c0 * 32; i < c0 * 32 + 32; i += 4) {
+              add2(c0s, c1s, c0s, c1s, eq_one(sv[i], bm), eq_one(sv[i + 1], bm));
+              add2(c2s, c3s, c2s, c3s, eq_one(sv[i + 2], bm), eq_one(sv[i + 3], bm));
             }
           }
-          bc = (bm == -INFINITY) ? 0 : (int)((c0s + c1s) + (c2s + c3s));
-        } else if (kStable == 2 || __any_sync(0xffffffffu, bm >= rm)) {
-          // each equality gives 1.0, summed in FP32 pairs (exact)
-          float c0s = 0.f, c1s = 0.f, c2s = 0.f, c3s = 0.f;
-#pragma unroll
-          for (int i = 0; i < kBlockN; i += 4) {
-            add2(c0s, c1s, c0s, c1s, eq_one(sv[i], bm), eq_one(sv[i + 1], bm));
-            add2(c2s, c3s, c2s, c3s, eq_one(sv[i + 2], bm), eq_one(sv[i + 3], bm));
-          }
-          bc = (bm == -INFINITY) ? 0 : (int)((c0s + c1s) + (c2s + c3s));
         }
+        bc = (bm == -INFINITY) ? 0 : (int)((c0s + c1s) + (c2s + c3s));
         const float rm_new = fmaxf(rm, bm);
         rs = ((rm == rm_new) ? rs : 0) + ((bm == rm_new) ? bc : 0);
         rm = rm_new;
