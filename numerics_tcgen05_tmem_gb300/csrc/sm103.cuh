@@ -143,19 +143,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-// One bounded probe of a phase: the thread may be suspended until the phase completes or
-// about kWaitHintNs pass.  A 1 us hint lets a waiting warp sleep instead of spending issue
-// slots in a polling loop beside the warps that compute (forward +0.5-3 % measured); 10 us
-// slowed the backward's hand-offs by 2-5 %.
-constexpr uint32_t kWaitHintNs = 1000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "n"(kWaitHintNs)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
